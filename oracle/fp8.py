@@ -1,0 +1,78 @@
+"""FP8 E4M3 codec and per-tensor absmax scaling (oracle; test infrastructure only).
+
+The whisper-blaze showcase site, "The Solution" (fp8_quantize.cu card:
+per-tensor scale, amax) and "Learnings" (E4M3 saturates at 448; scales come
+from activation maxima), and the PyPI page, "Direct Kernel API"
+(quantise_e4m3 returns codes and a per-tensor scale).
+
+Format (OCP 8-bit floating point, E4M3 "fn" variant): sign bit, 4 exponent
+bits with bias 7, 3 mantissa bits; exponent field 0 encodes subnormals
+m * 2^-9; S.1111.111 is NaN; there are no infinities; the largest finite
+magnitude is 1.75 * 2^8 = 448.
+
+Reading where the pages are silent: rounding is to nearest, ties to the even
+code; magnitudes above 448 (and infinities) saturate to 448; NaN stays NaN.
+The scaling recipe (taken in float32, the precision the GPU path uses):
+    amax  = max |x|                  (float32)
+    scale = amax / 448               (dequantisation scale; 1 when amax == 0)
+    inv   = 448 / amax               (1 when amax == 0)
+    code  = e4m3(float32(x) * inv)   (one float32 multiply, then RNE + saturate)
+Dequantisation is decode(code) * scale.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+NAN_CODE = 0x7F
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Exact float64 value of each 8-bit code."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((c & 0x7F) == NAN_CODE, np.nan, val)
+    return sign * val
+
+
+# Non-negative finite values in code order 0x00 .. 0x7E (monotonic in the code).
+_POS_VALUES = e4m3_decode(np.arange(0x7F))
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round each value to E4M3: nearest, ties to even code, saturate to +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    hi = np.searchsorted(_POS_VALUES, ax, side="left")      # first value >= ax
+    hi = np.minimum(hi, len(_POS_VALUES) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = ax - _POS_VALUES[lo]
+    d_hi = _POS_VALUES[hi] - ax
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(ax >= E4M3_MAX, 0x7E, code)               # saturate (incl. +inf)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), NAN_CODE, code)
+    return code.astype(np.uint8)
+
+
+def absmax_scale(x):
+    """(amax, scale, inv) of the per-tensor recipe, all float32."""
+    amax = np.float32(np.max(np.abs(np.asarray(x, dtype=np.float32)))) if np.size(x) else np.float32(0)
+    if amax == 0:
+        return amax, np.float32(1.0), np.float32(1.0)
+    return amax, np.float32(amax / np.float32(E4M3_MAX)), np.float32(np.float32(E4M3_MAX) / amax)
+
+
+def quantize(x):
+    """Per-tensor E4M3 quantisation: (codes uint8, scale float32)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    _, scale, inv = absmax_scale(x32)
+    return e4m3_encode((x32 * inv).astype(np.float32)), scale
+
+
+def dequantize(codes, scale) -> np.ndarray:
+    return e4m3_decode(codes) * np.float64(scale)
