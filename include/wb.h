@@ -1,0 +1,202 @@
+/*
+ * wb.h - C ABI of libwb, the GB300 (sm_103a) hot path of batched Whisper
+ * large-v3 encoding: float32 16 kHz audio -> log-mel -> conv stem -> encoder
+ * hidden states, with a per-layer-site precision choice (bf16 or FP8 E4M3).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor arguments are DEVICE pointers owned by the caller; libwb never
+ *    allocates or frees memory.  Scratch memory is passed in as a workspace
+ *    whose size the matching *_workspace_bytes() query returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and stream-ordered with the caller's other work.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned synchronously (WB_EINVAL, WB_EUNSUPPORTED, WB_EWORKSPACE).
+ *    Launch failures return WB_ECUDA.  Faults found on the device (a bounded
+ *    wait that ran out) are recorded in a device error word and reported by
+ *    wb_check_device_error().  No kernel traps.
+ *  - Pointers must be 16-byte aligned.  bf16 tensors hold IEEE bfloat16 bit
+ *    patterns; E4M3 tensors hold OCP FP8 E4M3 ("fn") codes.
+ *  - Row-major layouts throughout; "[a, b]" means b is contiguous.
+ *
+ * Sources (the pages this library follows): the whisper-blaze PyPI page
+ * ("Quick Start", "Batch Transcription", "Direct Kernel API") and the
+ * whisper-blaze showcase site ("The Approach", "The Solution", "Learnings").
+ */
+#ifndef WB_H
+#define WB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WB_OK = 0,
+  WB_EINVAL = -1,        /* bad pointer, size or layout argument */
+  WB_ECUDA = -2,         /* a CUDA runtime/driver call or launch failed */
+  WB_EUNSUPPORTED = -3,  /* valid request this build does not implement (e.g. mixed bf16 x E4M3 site) */
+  WB_ETIMEOUT = -4,      /* a bounded device-side wait ran out (reported by wb_check_device_error) */
+  WB_EWORKSPACE = -5     /* workspace pointer null or smaller than the *_workspace_bytes() query */
+} wb_status;
+
+/* Element types of one precision site (showcase site, "The Approach": a
+ * PrecisionConfig assigns weight and activation precision per layer site). */
+typedef enum { WB_BF16 = 0, WB_E4M3 = 1 } wb_dtype;
+
+/* The three encoder layer sites of the showcase site's precision table
+ * ("The Approach"): encoder_attn_qkv, encoder_attn_out, encoder_ffn (FC1 and
+ * FC2).  Weight and activation of one site must have the same type (the
+ * tensor core multiplies bf16 by bf16 or E4M3 by E4M3); a mixed site returns
+ * WB_EUNSUPPORTED.  Presets: all WB_BF16 ("full" precision, bf16 replacing
+ * the pages' fp16), and mixed_fp8 = qkv and ffn E4M3, out bf16. */
+typedef struct {
+  int32_t qkv_w, qkv_a;
+  int32_t out_w, out_a;
+  int32_t ffn_w, ffn_a;
+} wb_precision;
+
+/* Encoder shape.  large-v3: {128, 1280, 20, 32, 5120}; the tiny test shape
+ * {80, 384, 6, 1, 1536}.  Requires d_model = 64 * n_heads, d_model and d_ffn
+ * multiples of 64, 8 <= n_mels <= 128 and n_mels a multiple of 8. */
+typedef struct {
+  int32_t n_mels, d_model, n_heads, n_layers, d_ffn;
+} wb_dims;
+
+/* Conv stem weights.  Conv weights are bf16 in TAP-MAJOR layout
+ * [3][d_model][c_in] (produce it from the PyTorch layout [c_out][c_in][3]
+ * with wb_pack_conv_weight); biases are float32 [d_model]. */
+typedef struct {
+  const void* conv1_w;   /* bf16 [3][d][n_mels] */
+  const float* conv1_b;  /* [d] */
+  const void* conv2_w;   /* bf16 [3][d][d] */
+  const float* conv2_b;  /* [d] */
+} wb_stem_weights;
+
+/* One encoder layer.  Linear weights use the PyTorch/HF layout [out, in].
+ * w_qkv is the row concatenation of W_q, W_k, W_v ([3d, d]); b_qkv = [b_q, 0,
+ * b_v] (Whisper's key projection has no bias).  A weight stored as E4M3 comes
+ * with its float32 dequantisation scale s_* (a DEVICE scalar, as written by
+ * wb_quantize_fp8); for bf16 weights s_* is ignored and may be NULL.
+ * LayerNorm parameters and biases are float32. */
+typedef struct {
+  const float* ln1_g;
+  const float* ln1_b;
+  const void* w_qkv;  const float* b_qkv;  const float* s_qkv;  /* [3d, d], [3d] */
+  const void* w_out;  const float* b_out;  const float* s_out;  /* [d, d],  [d]  */
+  const float* ln2_g;
+  const float* ln2_b;
+  const void* w_fc1;  const float* b_fc1;  const float* s_fc1;  /* [F, d],  [F]  */
+  const void* w_fc2;  const float* b_fc2;  const float* s_fc2;  /* [d, F],  [d]  */
+} wb_layer_weights;
+
+typedef struct {
+  const float* g;
+  const float* b;
+} wb_ln_weights;
+
+/* ------------------------------------------------------------------------ */
+
+/* Human-readable name of a status code (static string). */
+const char* wb_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int wb_version(void);
+
+/* Synchronizes `stream`, then reads and clears this device's error word.
+ * Returns WB_ETIMEOUT if any kernel recorded a bounded-wait timeout since the
+ * last call, WB_ECUDA if the synchronization itself failed, else WB_OK.
+ * *detail (optional) receives the raw word (bits 8..15: the wait site). */
+wb_status wb_check_device_error(void* stream, uint32_t* detail);
+
+/* --- log-mel front end -----------------------------------------------------
+ * The showcase site, "The Solution" (mel_spectrogram.cu card: STFT, mel
+ * filterbank, overlapping-chunk mode for long audio) and the PyPI page,
+ * "Quick Start" (float32 mono audio at 16 kHz).
+ *
+ * Chunk c covers samples [c*chunk_stride, c*chunk_stride + 480000) of
+ * `audio`, zero-filled past n_samples (chunk_stride = 480000 for a batch of
+ * independent 30 s chunks stored back to back; 400000 for 30 s windows at a
+ * 25 s stride over one long recording).  Per chunk: reflect pad 200, periodic
+ * Hann n_fft 400, hop 160, power spectrum of frames 0..2999 (the last frame
+ * is dropped), Slaney mel filterbank over 0-8 kHz, log10(max(., 1e-10)),
+ * clamp to (chunk max - 8), then (x + 4) / 4.
+ * out: float32 [n_chunks, n_mels, 3000].  n_chunks = 0 is a no-op.
+ * Mono only: average multi-channel audio before the call. */
+size_t wb_logmel_workspace_bytes(int n_chunks, int n_mels);
+wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride, int n_chunks, int n_mels,
+                    float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* --- conv stem ---------------------------------------------------------------
+ * x0[b] = GELU(conv2(GELU(conv1(logmel[b])))) + sinusoidal positions, with
+ * conv1 = Conv1d(n_mels -> d, k3, stride 1, pad 1) and conv2 = Conv1d(d -> d,
+ * k3, stride 2, pad 1), computed as implicit GEMMs on the tensor cores
+ * (bf16 operands, fp32 accumulation, exact-erf GELU).
+ * logmel: float32 [batch, n_mels, 3000]; x0: bf16 [batch, 1500, d]. */
+size_t wb_conv_stem_workspace_bytes(const wb_dims* dims, int batch);
+wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, const wb_stem_weights* w, void* x0,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Reorders a PyTorch Conv1d weight (float32 [c_out][c_in][3]) into the
+ * tap-major bf16 layout [3][c_out][c_in] that wb_stem_weights expects. */
+wb_status wb_pack_conv_weight(const float* w, int c_out, int c_in, void* packed, void* stream);
+
+/* --- encoder -----------------------------------------------------------------
+ * Runs pre-LN encoder layers [layer_begin, layer_end) of `layers` on x0
+ * (bf16 [batch, 1500, d]) and, if apply_final_ln, the final LayerNorm
+ * (ln_post); writes bf16 [batch, 1500, d] to `out` (which must not alias x0).
+ * Per layer: h += OutProj(Attn(QKV(LN1(h)))); h += FC2(GELU(FC1(LN2(h)))),
+ * LayerNorm eps 1e-5 (PyPI page, "Direct Kernel API"), softmax attention over
+ * all 1500 positions with scale 1/8, exact-erf GELU.  `precision` selects the
+ * operand type of each site; an E4M3 activation is quantised on the device
+ * with one per-tensor absmax scale over the whole [batch*1500, k] operand of
+ * the call (showcase site, "Learnings": scales from activation maxima).
+ * layers[i] is read only for begin <= i < end. */
+size_t wb_encoder_workspace_bytes(const wb_dims* dims, int batch, const wb_precision* precision);
+wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, const wb_layer_weights* layers,
+                             const wb_ln_weights* ln_post, const wb_precision* precision, int layer_begin,
+                             int layer_end, int apply_final_ln, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* --- FP8 E4M3 ------------------------------------------------------------------
+ * PyPI page, "Direct Kernel API" (quantise_e4m3 / dequantise_e4m3) and the
+ * showcase site, "The Solution" (fp8_quantize.cu: per-tensor scale, amax).
+ * quantize: amax = max|x| over the n bf16 values, inv = 448 / amax, code =
+ * E4M3(x * inv) rounded to nearest even and saturated to +-448; *scale (a
+ * DEVICE float) receives amax / 448 (1 when amax = 0).  dequantize: y =
+ * decode(q) * (*scale) as bf16. */
+wb_status wb_quantize_fp8(const void* x, int64_t n, uint8_t* q, float* scale, void* stream);
+wb_status wb_dequantize_fp8(const uint8_t* q, const float* scale, int64_t n, void* y, void* stream);
+
+/* --- building blocks (exposed for unit tests and custom pipelines) ------------
+ * wb_linear: out[m, n] = act(alpha * sum_k a[m, k] w[n, k] + bias[n]) + resid[m, n]
+ * with alpha = (*scale_a) * (*scale_w) for E4M3 operands (both must then be
+ * given) and 1 for bf16; act = exact-erf GELU when gelu != 0.  a: [M, K],
+ * w: [N, K] (bf16 or E4M3 per `dtype`), bias float32 [N] or NULL, resid bf16
+ * [M, N] or NULL, out bf16 [M, N].  N must be a multiple of 32 and K a
+ * multiple of 8 (bf16) or 16 (E4M3). */
+wb_status wb_linear(const void* a, const void* w, int M, int N, int K, int dtype, const float* bias,
+                    const float* scale_a, const float* scale_w, int gelu, const void* resid, void* out,
+                    void* stream);
+
+/* Fused residual + LayerNorm (PyPI page, "Direct Kernel API":
+ * layernorm_fused / layernorm_fused_residual): total = x + residual,
+ * y = (total - mean) / sqrt(var + eps) * g + b over rows of width d (biased
+ * variance).  residual and total may be NULL.  x, residual, total, y: bf16
+ * [rows, d]; g, b: float32 [d].  d must be a multiple of 128 and <= 2048. */
+wb_status wb_layernorm(const void* x, const void* residual, const float* g, const float* b, int rows, int d,
+                       float eps, void* y, void* total, void* stream);
+
+/* Softmax attention without a mask (the encoder's self-attention):
+ * out[b, t, h*64:(h+1)*64] = softmax(q_h k_h^T / 8) v_h for every batch item
+ * and head.  q, k, v, out: bf16 [batch, T, 64*n_heads].  Needs a workspace of
+ * wb_attention_workspace_bytes() for the transposed V. */
+size_t wb_attention_workspace_bytes(int batch, int T, int n_heads);
+wb_status wb_attention(const void* q, const void* k, const void* v, int batch, int T, int n_heads, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WB_H */

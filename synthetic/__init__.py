@@ -112,24 +112,24 @@ def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
         return x
     if dtype != "bf16":
         raise ValueError(dtype)
-    u = x.view(np.uint32).astype(np.uint64)
-    # round-to-nearest-even on the upper 16 bits (inputs here are finite)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    import torch   # a storage-format conversion, not part of the method
+    return torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
 
 
 def _normal(rng, shape, std=0.02):
     return rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
 
 
-def encoder_weights(dims: Dims, seed: int, dtype: str = "bf16") -> dict:
+def encoder_weights(dims: Dims, seed: int, dtype: str = "bf16", n_layers: int | None = None) -> dict:
     """Random-init encoder weights in the HF Whisper layout.
 
     Returns {"conv1_w": [d, C, 3], "conv1_b": [d], "conv2_w": [d, d, 3],
     "conv2_b": [d], "layers": [dict per layer], "ln_post_g", "ln_post_b"}.
     Per layer: ln1_g, ln1_b, wq [d,d], bq, wk [d,d], wv [d,d], bv, wo [d,d],
     bo, ln2_g, ln2_b, w1 [F,d], b1 [F], w2 [d,F], b2 [d].  The k projection
-    has no bias.  All float32 arrays holding values of ``dtype``.
+    has no bias.  All float32 arrays holding values of ``dtype``.  With
+    ``n_layers`` < dims.n_layers only the first layers are drawn (identical to
+    the full draw's first layers) and the final LayerNorm is omitted.
     """
     rng = np.random.default_rng(seed)
     d, C, F = dims.d_model, dims.n_mels, dims.d_ffn
@@ -140,7 +140,8 @@ def encoder_weights(dims: Dims, seed: int, dtype: str = "bf16") -> dict:
     w["conv2_w"] = r(_normal(rng, (d, d, 3)))
     w["conv2_b"] = r(_normal(rng, (d,)))
     layers = []
-    for _ in range(dims.n_layers):
+    count = dims.n_layers if n_layers is None else n_layers
+    for _ in range(count):
         L = {}
         L["ln1_g"] = r(1.0 + _normal(rng, (d,)))
         L["ln1_b"] = r(_normal(rng, (d,)))
@@ -159,8 +160,9 @@ def encoder_weights(dims: Dims, seed: int, dtype: str = "bf16") -> dict:
         L["b2"] = r(_normal(rng, (d,)))
         layers.append(L)
     w["layers"] = layers
-    w["ln_post_g"] = r(1.0 + _normal(rng, (d,)))
-    w["ln_post_b"] = r(_normal(rng, (d,)))
+    if count == dims.n_layers:
+        w["ln_post_g"] = r(1.0 + _normal(rng, (d,)))
+        w["ln_post_b"] = r(_normal(rng, (d,)))
     return w
 
 

@@ -1,0 +1,141 @@
+"""Kernel-level parity of libwb against the oracle, through the C ABI (GPU).
+
+GEMMs on small-integer operands are bit-exact (bf16 and E4M3 hold small
+integers exactly and the fp32 accumulation of the products is exact); the
+other kernels are compared with the oracle's float64 results on seeded inputs
+at sizes that span several tiles plus a ragged tail."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import rel_l2, to_np
+from oracle import encoder as oenc
+from oracle import fp8 as ofp8
+import synthetic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _bf16(a):
+    return torch.as_tensor(np.asarray(a, np.float32)).to(DEV).to(torch.bfloat16)
+
+
+def _f32(a):
+    return torch.as_tensor(np.asarray(a, np.float32)).to(DEV)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 256, 320), (128, 384, 64), (1000, 1152, 384), (1, 32, 8), (4100, 512, 1280)])
+def test_linear_bf16_small_integers_bit_exact(wb, M, N, K):
+    a, w = synthetic.gemm_operands(M * 7 + N, M, N, K, -1, 1)
+    rng = np.random.default_rng(K)
+    bias = rng.integers(-4, 5, N).astype(np.float32)
+    resid = rng.integers(-4, 5, (M, N)).astype(np.float32)
+    ref = a.astype(np.int64) @ w.astype(np.int64).T + bias.astype(np.int64) + resid.astype(np.int64)
+    assert np.abs(ref).max() <= 256                       # representable exactly in bf16
+    out = wb.linear(_bf16(a), _bf16(w), bias=_f32(bias), resid=_bf16(resid))
+    assert wb.check_device_error() == 0
+    np.testing.assert_array_equal(to_np(out), ref.astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 256, 256), (257, 1280, 640)])
+def test_linear_e4m3_small_integers_bit_exact(wb, M, N, K):
+    a, w = synthetic.gemm_operands(5 * M + K, M, N, K, -2, 2)
+    qa = torch.as_tensor(ofp8.e4m3_encode(a)).to(DEV)
+    qw = torch.as_tensor(ofp8.e4m3_encode(w)).to(DEV)
+    one = torch.ones(1, dtype=torch.float32, device=DEV)
+    half = torch.full((1,), 0.5, dtype=torch.float32, device=DEV)
+    out = wb.linear(qa, qw, scale_a=one, scale_w=half)
+    ref = (a.astype(np.int64) @ w.astype(np.int64).T) * 0.5
+    assert np.abs(ref).max() <= 256
+    np.testing.assert_array_equal(to_np(out), ref)
+
+
+def test_linear_gelu_bias_matches_oracle(wb):
+    rng = np.random.default_rng(3)
+    M, N, K = 700, 1536, 384
+    a = synthetic.round_to(rng.normal(size=(M, K)).astype(np.float32), "bf16")
+    w = synthetic.round_to((rng.normal(size=(N, K)) * 0.05).astype(np.float32), "bf16")
+    b = rng.normal(size=N).astype(np.float32) * 0.1
+    out = wb.linear(_bf16(a), _bf16(w), bias=_f32(b), gelu=True)
+    ref = oenc.gelu(a.astype(np.float64) @ w.astype(np.float64).T + b)
+    assert rel_l2(to_np(out), ref) < 4e-3
+
+
+def test_fp8_gemm_matches_dequantized_operands(wb):
+    # E4M3 GEMM vs an fp64 GEMM of the dequantised (exactly representable) operands
+    rng = np.random.default_rng(4)
+    M, N, K = 513, 768, 1024
+    a = rng.normal(size=(M, K)).astype(np.float32)
+    w = (rng.normal(size=(N, K)) * 0.02).astype(np.float32)
+    qa, sa = wb.quantize_fp8(_bf16(a))
+    qw, sw = wb.quantize_fp8(_bf16(w))
+    out = wb.linear(qa, qw, scale_a=sa, scale_w=sw)
+    da = ofp8.dequantize(qa.cpu().numpy(), sa.item())
+    dw = ofp8.dequantize(qw.cpu().numpy(), sw.item())
+    ref = da @ dw.T
+    # the output is bf16: compare with the exact product rounded to bf16 (that
+    # rounding alone is ~1.1e-3 relative L2, so it cannot be part of the budget)
+    assert rel_l2(to_np(out), synthetic.round_to(ref.astype(np.float32), "bf16")) < 1e-3
+    assert rel_l2(to_np(out), ref) < 2.5e-3
+
+
+@pytest.mark.parametrize("n", [16, 4096 * 33 + 7, 1280 * 1500])
+def test_quantize_fp8_bit_exact_vs_oracle_codec(wb, n):
+    rng = np.random.default_rng(n)
+    x = synthetic.round_to((rng.normal(size=n) * 3.0).astype(np.float32), "bf16")
+    x[n // 3] = -11.5
+    q, s = wb.quantize_fp8(_bf16(x))
+    q_ref, s_ref = ofp8.quantize(x)
+    assert s.item() == float(s_ref)
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    y = wb.dequantize_fp8(q, s)
+    np.testing.assert_array_equal(to_np(y), synthetic.round_to(ofp8.dequantize(q_ref, s_ref).astype(np.float32), "bf16"))
+
+
+def test_quantize_zero_tensor_scale_one(wb):
+    q, s = wb.quantize_fp8(torch.zeros(64, dtype=torch.bfloat16, device=DEV))
+    assert s.item() == 1.0 and int(q.sum()) == 0
+
+
+@pytest.mark.parametrize("d,rows", [(1280, 3001), (384, 1500), (512, 7)])
+def test_layernorm_matches_oracle(wb, d, rows):
+    rng = np.random.default_rng(d)
+    x = synthetic.round_to(rng.normal(0.3, 2.0, size=(rows, d)).astype(np.float32), "bf16")
+    r = synthetic.round_to(rng.normal(size=(rows, d)).astype(np.float32), "bf16")
+    g = (1 + 0.1 * rng.normal(size=d)).astype(np.float32)
+    b = (0.1 * rng.normal(size=d)).astype(np.float32)
+    y, tot = wb.layernorm(_bf16(x), _f32(g), _f32(b), 1e-5, residual=_bf16(r), return_total=True)
+    ref = oenc.layer_norm(x.astype(np.float64) + r, g, b)
+    assert np.abs(to_np(y) - ref).max() < 0.02 * np.abs(ref).max() / 4
+    assert rel_l2(to_np(y), ref) < 4e-3
+    np.testing.assert_array_equal(to_np(tot), synthetic.round_to((x + r).astype(np.float32), "bf16"))
+    y2 = wb.layernorm(_bf16(x), _f32(g), _f32(b), 1e-5)
+    assert rel_l2(to_np(y2), oenc.layer_norm(x.astype(np.float64), g, b)) < 4e-3
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 1500, 2), (2, 130, 3), (1, 64, 1), (1, 257, 2)])
+def test_attention_matches_oracle(wb, B, T, H):
+    rng = np.random.default_rng(T + H)
+    d = 64 * H
+    q, k, v = (synthetic.round_to(rng.normal(size=(B, T, d)).astype(np.float32), "bf16") for _ in range(3))
+    out = to_np(wb.attention(_bf16(q), _bf16(k), _bf16(v), H))
+    assert wb.check_device_error() == 0
+    for b in range(B):
+        ref = oenc.attention(q[b].astype(np.float64), k[b], v[b], H)
+        assert rel_l2(out[b], ref) < 1e-2
+
+
+def test_attention_peaked_scores(wb):
+    # large-magnitude scores exercise the running-max rescale across key tiles
+    rng = np.random.default_rng(11)
+    B, T, H = 1, 700, 1
+    q = synthetic.round_to((rng.normal(size=(B, T, 64)) * 3).astype(np.float32), "bf16")
+    k = synthetic.round_to((rng.normal(size=(B, T, 64)) * 3).astype(np.float32), "bf16")
+    v = synthetic.round_to(rng.normal(size=(B, T, 64)).astype(np.float32), "bf16")
+    out = to_np(wb.attention(_bf16(q), _bf16(k), _bf16(v), H))
+    assert rel_l2(out[0], oenc.attention(q[0].astype(np.float64), k[0], v[0], H)) < 1e-2
+
+
+def test_device_error_word_clear(wb):
+    assert wb.check_device_error() == 0

@@ -1,0 +1,111 @@
+"""End-to-end parity of the hot path against the oracle through the C ABI (GPU):
+log-mel (max abs <= 1e-3), conv stem, encoder layers (relative L2 <= 1e-2 per
+layer, <= 3e-2 after the final LayerNorm, <= 6e-2 for mixed_fp8), on the
+seeded synthetic workloads."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import rel_l2, to_np
+from oracle import encoder as oenc
+from oracle import frontend as ofe
+import synthetic
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+LOGMEL_TOL = 1e-3
+LAYER_TOL = 1e-2
+FINAL_TOL = 3e-2
+FP8_TOL = 6e-2
+
+
+def _dev(a):
+    return torch.as_tensor(np.ascontiguousarray(a, dtype=np.float32)).to(DEV)
+
+
+@pytest.mark.parametrize("n_mels", [80, 128])
+def test_logmel_matches_oracle(wb, n_mels):
+    audio = synthetic.tone_batch(synthetic.SEED_TINY + 50, 3)
+    audio[2] = synthetic.half_silence(77)                   # clamp active on the last chunk
+    mel = to_np(wb.logmel(_dev(audio.reshape(-1)), 3, n_mels))
+    assert wb.check_device_error() == 0
+    for b in range(3):
+        ref = ofe.log_mel(audio[b], n_mels)
+        assert np.abs(mel[b] - ref).max() <= LOGMEL_TOL, b
+
+
+def test_logmel_silence_and_long_form_windows(wb):
+    # 1.3 M samples at a 25 s stride -> 4 windows, the last one zero-filled
+    x = synthetic.long_audio(synthetic.SEED_LONGFORM, 1_300_000)
+    n = ofe.n_chunks_for(len(x))
+    mel = to_np(wb.logmel(_dev(x), n, 128, chunk_stride=ofe.CHUNK_STRIDE))
+    chunks = ofe.chunk_audio(x)
+    for c in range(n):
+        assert np.abs(mel[c] - ofe.log_mel(chunks[c], 128)).max() <= LOGMEL_TOL, c
+    z = to_np(wb.logmel(_dev(np.zeros(480000)), 1, 80))
+    assert np.all(z == -1.5)
+
+
+def _tiny():
+    dims = synthetic.TINY
+    w = synthetic.encoder_weights(dims, synthetic.SEED_TINY, "f32")
+    return dims, w
+
+
+def test_conv_stem_matches_oracle(wb):
+    dims, w = _tiny()
+    stem, _ = wb.upload_weights(w)
+    rng = np.random.default_rng(0)
+    mel = rng.uniform(-1.5, 1.5, size=(2, dims.n_mels, 3000)).astype(np.float32)
+    x0 = to_np(wb.conv_stem(_dev(mel), dims, stem))
+    for b in range(2):
+        assert rel_l2(x0[b], oenc.conv_stem(mel[b], w)) < LAYER_TOL
+
+
+def test_tiny_pipeline_matches_oracle(wb):
+    dims, w = _tiny()
+    stem, enc = wb.upload_weights(w)
+    audio = synthetic.tone_chunk(synthetic.SEED_TINY)[None]
+    pipe = wb.Pipeline(dims, stem, enc, batch=1)
+    out = to_np(pipe(_dev(audio.reshape(-1))))[0]
+    assert wb.check_device_error() == 0
+    ref_mel = ofe.log_mel(audio[0], dims.n_mels)
+    ref = oenc.encoder(oenc.conv_stem(ref_mel, w), w, dims.n_heads)
+    assert rel_l2(out, ref) < FINAL_TOL
+    # the layer output itself (no final LN), from the GPU's own stem output
+    x0 = wb.conv_stem(_dev(ref_mel[None]), dims, stem)
+    h = to_np(wb.encoder_forward(x0, dims, enc, final_ln=False))[0]
+    ref_h = oenc.encoder(to_np(x0)[0], w, dims.n_heads, final_ln=False)
+    assert rel_l2(h, ref_h) < LAYER_TOL
+
+
+def test_tiny_mixed_fp8(wb):
+    dims, w = _tiny()
+    _, enc = wb.upload_weights(w)
+    x0 = oenc.conv_stem(ofe.log_mel(synthetic.tone_chunk(5), dims.n_mels), w)
+    x0d = _dev(x0[None]).to(torch.bfloat16)
+    enc.quantize()
+    out = to_np(wb.encoder_forward(x0d, dims, enc, precision=wb.PRESET_MIXED_FP8))[0]
+    ref = oenc.encoder(to_np(x0d)[0], w, dims.n_heads)
+    assert rel_l2(out, ref) < FP8_TOL
+
+
+def test_encoder_zero_layers_and_range(wb):
+    dims, w = _tiny()
+    _, enc = wb.upload_weights(w)
+    x0 = torch.randn(2, 1500, dims.d_model, device=DEV).to(torch.bfloat16)
+    same = wb.encoder_forward(x0, dims, enc, layer_begin=0, layer_end=0, final_ln=False)
+    assert torch.equal(same, x0)
+    ln = to_np(wb.encoder_forward(x0, dims, enc, layer_begin=0, layer_end=0, final_ln=True))
+    ref = oenc.layer_norm(to_np(x0), w["ln_post_g"], w["ln_post_b"])
+    assert rel_l2(ln, ref) < 4e-3
+
+
+def test_encoder_is_deterministic(wb):
+    dims, w = _tiny()
+    _, enc = wb.upload_weights(w)
+    x0 = torch.randn(3, 1500, dims.d_model, device=DEV).to(torch.bfloat16)
+    a = wb.encoder_forward(x0, dims, enc)
+    b = wb.encoder_forward(x0, dims, enc)
+    assert torch.equal(a, b)

@@ -1,0 +1,10 @@
+"""GB300 (sm_103a) hot path of batched Whisper large-v3 encoding.
+
+libwb (CUDA, C ABI in include/wb.h) computes log-mel, the conv stem and the
+encoder layers on the tensor cores; this package builds it and binds it.
+"""
+from ._lib import WB_BF16, WB_E4M3, WbError, load  # noqa: F401
+from .api import (  # noqa: F401
+    PRESET_BF16, PRESET_MIXED_FP8, EncoderWeights, LayerWeights, Pipeline, StemWeights, attention,
+    check_device_error, conv_stem, dequantize_fp8, encoder_forward, encoder_workspace_bytes, layernorm, linear,
+    logmel, logmel_workspace_bytes, pack_conv_weight, quantize_fp8, upload_weights)

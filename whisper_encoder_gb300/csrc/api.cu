@@ -1,0 +1,667 @@
+// libwb C ABI: argument checks, workspace layout, TMA tensor maps and the
+// launch sequence of each entry point declared in include/wb.h.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/wb.h"
+#include "internal.h"
+
+using namespace wb;
+
+namespace {
+
+// ------------------------------ device error word --------------------------
+__device__ uint32_t g_err_word;
+
+constexpr int MAX_DEVICES = 64;
+uint32_t* g_err_ptr[MAX_DEVICES] = {nullptr};
+std::mutex g_mu;
+
+uint32_t* err_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+// ------------------------------ tensor maps --------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool encoder_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return true;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// rank-dimensional tiled map; strides in bytes for dims 1..rank-1; 128-byte swizzle.
+bool make_map(CUtensorMap* m, bool u8, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
+              const uint32_t* box) {
+  if (!encoder_fn()) return false;
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+  CUresult r = g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A operand view: (k, row, part, batch) with box (BK, 128, 1, 1).
+bool a_map(CUtensorMap* m, bool u8, const void* base, uint64_t k, uint64_t rows, uint64_t parts, uint64_t batch,
+           uint64_t row_stride, uint64_t part_stride, uint64_t batch_stride) {
+  const uint64_t dims[4] = {k, rows, parts, batch};
+  const uint64_t str[3] = {row_stride, part_stride, batch_stride};
+  const uint32_t box[4] = {u8 ? 128u : 64u, static_cast<uint32_t>(GEMM_BM), 1u, 1u};
+  return make_map(m, u8, 4, base, dims, str, box);
+}
+
+// B operand view: (k, n, part) with box (BK, BN, 1).
+bool b_map(CUtensorMap* m, bool u8, const void* base, uint64_t k, uint64_t n, uint64_t parts, uint64_t row_stride,
+           uint64_t part_stride, int bn) {
+  const uint64_t dims[3] = {k, n, parts};
+  const uint64_t str[2] = {row_stride, part_stride};
+  const uint32_t box[3] = {u8 ? 128u : 64u, static_cast<uint32_t>(bn), 1u};
+  return make_map(m, u8, 3, base, dims, str, box);
+}
+
+// ------------------------------ helpers ------------------------------------
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return o;
+  }
+};
+
+#define WB_CUDA(x)                         \
+  do {                                     \
+    if ((x) != cudaSuccess) return WB_ECUDA; \
+  } while (0)
+
+GemmParams base_params() {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = 1;
+  p.err = err_ptr();
+  return p;
+}
+
+void one_pass(GemmParams& p, int n_kb) {
+  p.n_pass = 1;
+  p.pass[0] = GemmPass{0, 0, 0, 0, 0, 0, static_cast<int16_t>(n_kb), 0};
+}
+
+// Plain GEMM out[M, N] = epilogue(A[M, K] . W[N, K]^T), A and W dense row-major.
+wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8, GemmParams p, cudaStream_t s) {
+  GemmLaunch g;
+  std::memset(&g, 0, sizeof(g));
+  const uint64_t es = fp8 ? 1 : 2;
+  g.bn = (N % 256 == 0 || N > 512) ? 256 : 128;
+  g.fp8 = fp8;
+  g.epi = EPI_STD;
+  if (!a_map(&g.amap[0], fp8, A, K, M, 1, 1, K * es, static_cast<uint64_t>(M) * K * es,
+             static_cast<uint64_t>(M) * K * es))
+    return WB_ECUDA;
+  g.amap[1] = g.amap[2] = g.amap[3] = g.amap[0];
+  if (!b_map(&g.bmap, fp8, W, K, N, 1, K * es, static_cast<uint64_t>(N) * K * es, g.bn)) return WB_ECUDA;
+  p.M = M;
+  p.N = N;
+  p.batch = 1;
+  const int bk = fp8 ? 128 : 64;
+  one_pass(p, (K + bk - 1) / bk);
+  g.p = p;
+  WB_CUDA(launch_gemm(g, s));
+  return WB_OK;
+}
+
+bool dims_ok(const wb_dims* d) {
+  return d && d->n_heads > 0 && d->d_model == 64 * d->n_heads && d->d_model % 64 == 0 && d->d_ffn > 0 &&
+         d->d_ffn % 64 == 0 && d->n_mels >= 8 && d->n_mels <= MEL_ROWS && d->n_mels % 8 == 0 && d->n_layers >= 0 &&
+         d->d_model <= 2048;
+}
+
+bool site_ok(int w, int a) { return (w == WB_BF16 || w == WB_E4M3) && w == a; }
+
+struct EncLayout {
+  size_t h, a, qk, vt, o, g, aq, gq, slots, total;
+};
+
+EncLayout enc_layout(const wb_dims* d, int batch, const wb_precision* pr) {
+  const size_t M = static_cast<size_t>(batch) * T_TOK;
+  const size_t D = d->d_model, F = d->d_ffn;
+  const bool any8 = pr && (pr->qkv_a == WB_E4M3 || pr->out_a == WB_E4M3 || pr->ffn_a == WB_E4M3);
+  const bool ffn8 = pr && pr->ffn_a == WB_E4M3;
+  Carver c;
+  EncLayout L;
+  L.h = c.take(M * D * 2);
+  L.a = c.take(M * D * 2);
+  L.qk = c.take(M * 2 * D * 2);
+  L.vt = c.take(static_cast<size_t>(batch) * d->n_heads * 64 * T_PAD * 2);
+  L.o = c.take(M * D * 2);
+  L.g = c.take(M * F * 2);
+  L.aq = any8 ? c.take(M * D) : 0;
+  L.gq = ffn8 ? c.take(M * F) : 0;
+  L.slots = c.take(static_cast<size_t>(8) * (d->n_layers > 0 ? d->n_layers : 1) * sizeof(float));
+  L.total = c.off;
+  return L;
+}
+
+struct MelLayout {
+  size_t xs, basis, pw, fbs, mmax, total;
+};
+
+MelLayout mel_layout(int n_chunks) {
+  Carver c;
+  MelLayout L;
+  L.xs = c.take(static_cast<size_t>(n_chunks) * 3 * PADDED * 2);
+  L.basis = c.take(static_cast<size_t>(3) * DFT_ROWS * N_FFT * 2);
+  L.pw = c.take(static_cast<size_t>(n_chunks) * 2 * N_FRAMES * N_BIN_PAD * 2);
+  L.fbs = c.take(static_cast<size_t>(2) * MEL_ROWS * N_BIN_PAD * 2);
+  L.mmax = c.take(static_cast<size_t>(n_chunks) * sizeof(float));
+  L.total = c.off;
+  return L;
+}
+
+struct StemLayout {
+  size_t yTp, y1p, total;
+};
+
+StemLayout stem_layout(const wb_dims* d, int batch) {
+  Carver c;
+  StemLayout L;
+  L.yTp = c.take(static_cast<size_t>(batch) * (N_FRAMES + 2) * d->n_mels * 2);
+  L.y1p = c.take(static_cast<size_t>(batch) * (N_FRAMES + 1) * d->d_model * 2);
+  L.total = c.off;
+  return L;
+}
+
+// Attention over q/k row views (row stride ld_qk elements) and V^T.
+wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long long ld_qk, const __nv_bfloat16* vt,
+                        int batch, int T, int H, __nv_bfloat16* out, cudaStream_t s) {
+  const uint64_t d = static_cast<uint64_t>(H) * 64;
+  CUtensorMap qm, km, vm;
+  const uint64_t qdims[3] = {d, static_cast<uint64_t>(T), static_cast<uint64_t>(batch)};
+  const uint64_t qstr[2] = {static_cast<uint64_t>(ld_qk) * 2, static_cast<uint64_t>(ld_qk) * 2 * T};
+  const uint32_t qbox[3] = {64, 128, 1};
+  if (!make_map(&qm, false, 3, q, qdims, qstr, qbox)) return WB_ECUDA;
+  if (!make_map(&km, false, 3, k, qdims, qstr, qbox)) return WB_ECUDA;
+  const uint64_t vdims[3] = {static_cast<uint64_t>(T), 64, static_cast<uint64_t>(batch) * H};
+  const uint64_t vstr[2] = {static_cast<uint64_t>(T_PAD) * 2, static_cast<uint64_t>(T_PAD) * 2 * 64};
+  const uint32_t vbox[3] = {64, 64, 1};
+  if (!make_map(&vm, false, 3, vt, vdims, vstr, vbox)) return WB_ECUDA;
+  AttnParams p;
+  p.T = T;
+  p.H = H;
+  p.d = static_cast<int>(d);
+  p.batch = batch;
+  p.scale_log2 = 1.4426950408889634f / 8.0f;
+  p.out = out;
+  p.err = err_ptr();
+  WB_CUDA(launch_attention(qm, km, vm, p, s));
+  return WB_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+const char* wb_status_string(int status) {
+  switch (status) {
+    case WB_OK: return "ok";
+    case WB_EINVAL: return "invalid argument";
+    case WB_ECUDA: return "CUDA error";
+    case WB_EUNSUPPORTED: return "unsupported configuration";
+    case WB_ETIMEOUT: return "device-side wait timed out";
+    case WB_EWORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int wb_version(void) { return 100; }
+
+wb_status wb_check_device_error(void* stream, uint32_t* detail) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return WB_ECUDA;
+  uint32_t* e = err_ptr();
+  if (!e) return WB_ECUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, e, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return WB_ECUDA;
+  if (word) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(e, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return WB_ECUDA;
+  }
+  if (detail) *detail = word;
+  return (word & ERR_TIMEOUT) ? WB_ETIMEOUT : WB_OK;
+}
+
+// ------------------------------- log-mel -----------------------------------
+size_t wb_logmel_workspace_bytes(int n_chunks, int n_mels) {
+  (void)n_mels;
+  return n_chunks > 0 ? mel_layout(n_chunks).total : 0;
+}
+
+wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride, int n_chunks, int n_mels,
+                    float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_chunks < 0 || n_mels < 8 || n_mels > MEL_ROWS || n_mels % 8 != 0 || n_samples < 0 || chunk_stride < 1)
+    return WB_EINVAL;
+  if (n_chunks == 0) return WB_OK;
+  if (!audio || !out || !aligned16(out) || !aligned16(audio)) return WB_EINVAL;
+  const MelLayout L = mel_layout(n_chunks);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < L.total) return WB_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto* xs = reinterpret_cast<__nv_bfloat16*>(ws + L.xs);
+  auto* basis = reinterpret_cast<__nv_bfloat16*>(ws + L.basis);
+  auto* pw = reinterpret_cast<__nv_bfloat16*>(ws + L.pw);
+  auto* fbs = reinterpret_cast<__nv_bfloat16*>(ws + L.fbs);
+  auto* mmax = reinterpret_cast<float*>(ws + L.mmax);
+
+  WB_CUDA(cudaMemsetAsync(mmax, 0, n_chunks * sizeof(float), s));
+  WB_CUDA(launch_dft_basis(basis, s));
+  WB_CUDA(launch_mel_fb(fbs, n_mels, s));
+  WB_CUDA(launch_pad_split(audio, n_samples, chunk_stride, n_chunks, xs, s));
+
+  // Windowed DFT: frames are read as four column segments of the padded
+  // signal (row t starts at sample 160 t), each times its slice of the basis,
+  // for the six leading products of the 3-way bf16 split.
+  {
+    GemmLaunch g;
+    std::memset(&g, 0, sizeof(g));
+    g.bn = 256;
+    g.fp8 = false;
+    g.epi = EPI_POWER;
+    for (int sgm = 0; sgm < 4; ++sgm) {
+      if (!a_map(&g.amap[sgm], false, xs + 128 * sgm, sgm < 3 ? 128 : 64, N_FRAMES, 3, n_chunks, HOP * 2,
+                 static_cast<uint64_t>(PADDED) * 2, static_cast<uint64_t>(PADDED) * 2 * 3))
+        return WB_ECUDA;
+    }
+    if (!b_map(&g.bmap, false, basis, N_FFT, DFT_ROWS, 3, N_FFT * 2, static_cast<uint64_t>(DFT_ROWS) * N_FFT * 2, 256))
+      return WB_ECUDA;
+    GemmParams p = base_params();
+    p.M = N_FRAMES;
+    p.N = DFT_ROWS;
+    p.batch = n_chunks;
+    const int pairs[6][2] = {{0, 0}, {0, 1}, {1, 0}, {0, 2}, {1, 1}, {2, 0}};
+    int np = 0;
+    for (int q = 0; q < 6; ++q)
+      for (int sgm = 0; sgm < 4; ++sgm)
+        p.pass[np++] = GemmPass{static_cast<int8_t>(sgm), static_cast<int8_t>(pairs[q][0]), 0,
+                                static_cast<int8_t>(pairs[q][1]), 0, static_cast<int16_t>(128 * sgm),
+                                static_cast<int16_t>(sgm < 3 ? 2 : 1), 0};
+    p.n_pass = np;
+    p.pw = pw;
+    p.pw_ld = N_BIN_PAD;
+    g.p = p;
+    WB_CUDA(launch_gemm(g, s));
+  }
+  // Mel filterbank: power (hi, lo) x filterbank (hi, lo), three leading products.
+  {
+    GemmLaunch g;
+    std::memset(&g, 0, sizeof(g));
+    g.bn = 128;
+    g.fp8 = false;
+    g.epi = EPI_MEL;
+    if (!a_map(&g.amap[0], false, pw, N_BIN_PAD, N_FRAMES, 2, n_chunks, N_BIN_PAD * 2,
+               static_cast<uint64_t>(N_FRAMES) * N_BIN_PAD * 2, static_cast<uint64_t>(N_FRAMES) * N_BIN_PAD * 4))
+      return WB_ECUDA;
+    g.amap[1] = g.amap[2] = g.amap[3] = g.amap[0];
+    if (!b_map(&g.bmap, false, fbs, N_BIN_PAD, MEL_ROWS, 2, N_BIN_PAD * 2,
+               static_cast<uint64_t>(MEL_ROWS) * N_BIN_PAD * 2, 128))
+      return WB_ECUDA;
+    GemmParams p = base_params();
+    p.M = N_FRAMES;
+    p.N = MEL_ROWS;
+    p.batch = n_chunks;
+    const int pairs[3][2] = {{0, 0}, {0, 1}, {1, 0}};
+    for (int q = 0; q < 3; ++q)
+      p.pass[q] = GemmPass{0, static_cast<int8_t>(pairs[q][0]), 0, static_cast<int8_t>(pairs[q][1]), 0, 0,
+                           N_BIN_PAD / 64, 0};
+    p.n_pass = 3;
+    p.mel_out = out;
+    p.mel_max = mmax;
+    p.n_valid = n_mels;
+    g.p = p;
+    WB_CUDA(launch_gemm(g, s));
+  }
+  WB_CUDA(launch_logmel_post(out, mmax, n_chunks, n_mels, s));
+  return WB_OK;
+}
+
+// ------------------------------- conv stem ---------------------------------
+size_t wb_conv_stem_workspace_bytes(const wb_dims* dims, int batch) {
+  if (!dims_ok(dims) || batch < 1) return 0;
+  return stem_layout(dims, batch).total;
+}
+
+wb_status wb_pack_conv_weight(const float* w, int c_out, int c_in, void* packed, void* stream) {
+  if (!w || !packed || c_out < 1 || c_in < 1) return WB_EINVAL;
+  WB_CUDA(launch_pack_conv(w, c_out, c_in, static_cast<__nv_bfloat16*>(packed), static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, const wb_stem_weights* w, void* x0,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dims_ok(dims) || batch < 0) return WB_EINVAL;
+  if (batch == 0) return WB_OK;
+  if (!logmel || !w || !w->conv1_w || !w->conv1_b || !w->conv2_w || !w->conv2_b || !x0 || !aligned16(x0) ||
+      !aligned16(w->conv1_w) || !aligned16(w->conv2_w))
+    return WB_EINVAL;
+  const StemLayout L = stem_layout(dims, batch);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < L.total) return WB_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto* yTp = reinterpret_cast<__nv_bfloat16*>(ws + L.yTp);
+  auto* y1p = reinterpret_cast<__nv_bfloat16*>(ws + L.y1p);
+  const int C = dims->n_mels, D = dims->d_model;
+  const int bn = (D % 256 == 0) ? 256 : 128;
+
+  WB_CUDA(launch_stem_transpose(logmel, batch, C, yTp, s));
+  WB_CUDA(launch_zero_rows(y1p, D, static_cast<long long>(N_FRAMES + 1) * D, batch, 0, s));
+  {  // conv1: three taps = three passes over row-shifted views of yTp
+    GemmLaunch g;
+    std::memset(&g, 0, sizeof(g));
+    g.bn = bn;
+    g.epi = EPI_STD;
+    const uint64_t rs = static_cast<uint64_t>(C) * 2, item = static_cast<uint64_t>(N_FRAMES + 2) * C * 2;
+    if (!a_map(&g.amap[0], false, yTp, C, N_FRAMES + 2, 1, batch, rs, item, item)) return WB_ECUDA;
+    g.amap[1] = g.amap[2] = g.amap[3] = g.amap[0];
+    if (!b_map(&g.bmap, false, w->conv1_w, C, D, 3, rs, static_cast<uint64_t>(D) * C * 2, bn)) return WB_ECUDA;
+    GemmParams p = base_params();
+    p.M = N_FRAMES;
+    p.N = D;
+    p.batch = batch;
+    for (int j = 0; j < 3; ++j)
+      p.pass[j] = GemmPass{0, 0, static_cast<int8_t>(j), static_cast<int8_t>(j), 0, 0,
+                           static_cast<int16_t>((C + 63) / 64), 0};
+    p.n_pass = 3;
+    p.out = y1p;
+    p.ldo = D;
+    p.out_batch_rows = N_FRAMES + 1;
+    p.out_row_off = 1;
+    p.bias = w->conv1_b;
+    p.act_gelu = 1;
+    g.p = p;
+    WB_CUDA(launch_gemm(g, s));
+  }
+  {  // conv2: stride 2 -> one tensor map per tap over every other row of y1p
+    GemmLaunch g;
+    std::memset(&g, 0, sizeof(g));
+    g.bn = bn;
+    g.epi = EPI_STD;
+    const uint64_t rs = static_cast<uint64_t>(2 * D) * 2;
+    for (int j = 0; j < 3; ++j)
+      if (!a_map(&g.amap[j], false, y1p + static_cast<long long>(j) * D, D, T_TOK, 1, batch, rs, rs * T_TOK,
+                 static_cast<uint64_t>(N_FRAMES + 1) * D * 2))
+        return WB_ECUDA;
+    g.amap[3] = g.amap[0];
+    if (!b_map(&g.bmap, false, w->conv2_w, D, D, 3, static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(D) * D * 2,
+               bn))
+      return WB_ECUDA;
+    GemmParams p = base_params();
+    p.M = T_TOK;
+    p.N = D;
+    p.batch = batch;
+    for (int j = 0; j < 3; ++j)
+      p.pass[j] = GemmPass{static_cast<int8_t>(j), 0, 0, static_cast<int8_t>(j), 0, 0, static_cast<int16_t>(D / 64), 0};
+    p.n_pass = 3;
+    p.out = x0;
+    p.ldo = D;
+    p.out_batch_rows = T_TOK;
+    p.bias = w->conv2_b;
+    p.act_gelu = 1;
+    p.add_pe = 1;
+    g.p = p;
+    WB_CUDA(launch_gemm(g, s));
+  }
+  return WB_OK;
+}
+
+// -------------------------------- encoder ----------------------------------
+size_t wb_encoder_workspace_bytes(const wb_dims* dims, int batch, const wb_precision* precision) {
+  if (!dims_ok(dims) || batch < 1) return 0;
+  return enc_layout(dims, batch, precision).total;
+}
+
+wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, const wb_layer_weights* layers,
+                             const wb_ln_weights* ln_post, const wb_precision* precision, int layer_begin,
+                             int layer_end, int apply_final_ln, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!dims_ok(dims) || batch < 0 || layer_begin < 0 || layer_end < layer_begin || layer_end > dims->n_layers)
+    return WB_EINVAL;
+  wb_precision pr = {WB_BF16, WB_BF16, WB_BF16, WB_BF16, WB_BF16, WB_BF16};
+  if (precision) pr = *precision;
+  if (!site_ok(pr.qkv_w, pr.qkv_a) || !site_ok(pr.out_w, pr.out_a) || !site_ok(pr.ffn_w, pr.ffn_a))
+    return WB_EUNSUPPORTED;
+  if (batch == 0) return WB_OK;
+  if (!x0 || !out || !aligned16(x0) || !aligned16(out) || x0 == out) return WB_EINVAL;
+  if (layer_end > layer_begin && !layers) return WB_EINVAL;
+  if (apply_final_ln && (!ln_post || !ln_post->g || !ln_post->b)) return WB_EINVAL;
+  for (int l = layer_begin; l < layer_end; ++l) {
+    const wb_layer_weights& L = layers[l];
+    if (!L.ln1_g || !L.ln1_b || !L.w_qkv || !L.b_qkv || !L.w_out || !L.b_out || !L.ln2_g || !L.ln2_b || !L.w_fc1 ||
+        !L.b_fc1 || !L.w_fc2 || !L.b_fc2)
+      return WB_EINVAL;
+    if ((pr.qkv_w == WB_E4M3 && !L.s_qkv) || (pr.out_w == WB_E4M3 && !L.s_out) ||
+        (pr.ffn_w == WB_E4M3 && (!L.s_fc1 || !L.s_fc2)))
+      return WB_EINVAL;
+  }
+  const EncLayout EL = enc_layout(dims, batch, &pr);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < EL.total) return WB_EWORKSPACE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int D = dims->d_model, F = dims->d_ffn, H = dims->n_heads;
+  const int M = batch * T_TOK;
+  auto* h = reinterpret_cast<__nv_bfloat16*>(ws + EL.h);
+  auto* a = reinterpret_cast<__nv_bfloat16*>(ws + EL.a);
+  auto* qk = reinterpret_cast<__nv_bfloat16*>(ws + EL.qk);
+  auto* vt = reinterpret_cast<__nv_bfloat16*>(ws + EL.vt);
+  auto* o = reinterpret_cast<__nv_bfloat16*>(ws + EL.o);
+  auto* g = reinterpret_cast<__nv_bfloat16*>(ws + EL.g);
+  auto* aq = EL.aq || pr.qkv_a == WB_E4M3 || pr.out_a == WB_E4M3 || pr.ffn_a == WB_E4M3
+                 ? reinterpret_cast<uint8_t*>(ws + EL.aq)
+                 : nullptr;
+  auto* gq = pr.ffn_a == WB_E4M3 ? reinterpret_cast<uint8_t*>(ws + EL.gq) : nullptr;
+  auto* slots = reinterpret_cast<float*>(ws + EL.slots);
+  const auto* x0b = static_cast<const __nv_bfloat16*>(x0);
+  auto* outb = static_cast<__nv_bfloat16*>(out);
+  const float eps = 1e-5f;
+  const int n_layers_run = layer_end - layer_begin;
+
+  if (n_layers_run > 0) WB_CUDA(cudaMemsetAsync(slots, 0, sizeof(float) * 8 * dims->n_layers, s));
+
+  for (int l = layer_begin; l < layer_end; ++l) {
+    const wb_layer_weights& W = layers[l];
+    float* sl = slots + 8 * l;  // [qkv amax, qkv scale, out amax, out scale, fc1 amax, fc1 scale, fc2 amax, fc2 scale]
+    const __nv_bfloat16* src = (l == layer_begin) ? x0b : h;
+    const bool last = (l == layer_end - 1);
+    const bool q8 = pr.qkv_a == WB_E4M3, o8 = pr.out_a == WB_E4M3, f8 = pr.ffn_a == WB_E4M3;
+
+    // LN1 -> a  [-> E4M3]
+    WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? sl + 0 : nullptr, s));
+    if (q8) WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 0, sl + 1, s));
+    {  // QKV projection: q | k to qk [M, 2D], v transposed to vt
+      GemmParams p = base_params();
+      p.out = qk;
+      p.ldo = 2 * D;
+      p.out_batch_rows = 0;
+      p.bias = W.b_qkv;
+      p.vt = vt;
+      p.vt_col0 = 2 * D;
+      p.vt_T = T_TOK;
+      p.vt_ld = T_PAD;
+      if (q8) {
+        p.scale_a = sl + 1;
+        p.scale_b = W.s_qkv;
+      }
+      wb_status st = dense_gemm(q8 ? static_cast<const void*>(aq) : a, W.w_qkv, M, 3 * D, D, q8, p, s);
+      if (st != WB_OK) return st;
+    }
+    {
+      wb_status st = run_attention(qk, qk + D, 2 * D, vt, batch, T_TOK, H, o, s);
+      if (st != WB_OK) return st;
+    }
+    if (o8) {
+      WB_CUDA(launch_amax(o, static_cast<long long>(M) * D, sl + 2, s));
+      WB_CUDA(launch_quantize(o, static_cast<long long>(M) * D, aq, sl + 2, sl + 3, s));
+    }
+    {  // out projection + bias + residual -> h
+      GemmParams p = base_params();
+      p.out = h;
+      p.ldo = D;
+      p.bias = W.b_out;
+      p.resid = src;
+      if (o8) {
+        p.scale_a = sl + 3;
+        p.scale_b = W.s_out;
+      }
+      wb_status st = dense_gemm(o8 ? static_cast<const void*>(aq) : o, W.w_out, M, D, D, o8, p, s);
+      if (st != WB_OK) return st;
+    }
+    // LN2 -> a [-> E4M3]
+    WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? sl + 4 : nullptr, s));
+    if (f8) WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 4, sl + 5, s));
+    {  // FC1 + bias + GELU -> g
+      GemmParams p = base_params();
+      p.out = g;
+      p.ldo = F;
+      p.bias = W.b_fc1;
+      p.act_gelu = 1;
+      if (f8) {
+        p.scale_a = sl + 5;
+        p.scale_b = W.s_fc1;
+        p.amax = sl + 6;
+      }
+      wb_status st = dense_gemm(f8 ? static_cast<const void*>(aq) : a, W.w_fc1, M, F, D, f8, p, s);
+      if (st != WB_OK) return st;
+    }
+    if (f8) WB_CUDA(launch_quantize(g, static_cast<long long>(M) * F, gq, sl + 6, sl + 7, s));
+    {  // FC2 + bias + residual -> h (or straight to out after the last layer without final LN)
+      GemmParams p = base_params();
+      p.out = (last && !apply_final_ln) ? outb : h;
+      p.ldo = D;
+      p.bias = W.b_fc2;
+      p.resid = h;
+      if (f8) {
+        p.scale_a = sl + 7;
+        p.scale_b = W.s_fc2;
+      }
+      wb_status st = dense_gemm(f8 ? static_cast<const void*>(gq) : g, W.w_fc2, M, D, F, f8, p, s);
+      if (st != WB_OK) return st;
+    }
+  }
+  const __nv_bfloat16* final_src = n_layers_run > 0 ? h : x0b;
+  if (apply_final_ln) {
+    WB_CUDA(launch_layernorm(final_src, nullptr, ln_post->g, ln_post->b, M, D, eps, outb, nullptr, nullptr, s));
+  } else if (n_layers_run == 0) {
+    WB_CUDA(cudaMemcpyAsync(outb, x0b, static_cast<size_t>(M) * D * 2, cudaMemcpyDeviceToDevice, s));
+  }
+  return WB_OK;
+}
+
+// --------------------------------- FP8 --------------------------------------
+wb_status wb_quantize_fp8(const void* x, int64_t n, uint8_t* q, float* scale, void* stream) {
+  if (n < 0 || !scale) return WB_EINVAL;
+  if (n > 0 && (!x || !q || !aligned16(x) || !aligned16(q))) return WB_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  WB_CUDA(cudaMemsetAsync(scale, 0, sizeof(float), s));
+  if (n > 0) {
+    WB_CUDA(launch_amax(xb, n, scale, s));
+    WB_CUDA(launch_quantize(xb, n, q, scale, nullptr, s));
+  }
+  WB_CUDA(launch_finalize_scale(scale, s));
+  return WB_OK;
+}
+
+wb_status wb_dequantize_fp8(const uint8_t* q, const float* scale, int64_t n, void* y, void* stream) {
+  if (n < 0 || !scale) return WB_EINVAL;
+  if (n == 0) return WB_OK;
+  if (!q || !y) return WB_EINVAL;
+  WB_CUDA(launch_dequantize(q, scale, n, static_cast<__nv_bfloat16*>(y), static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+// ------------------------------ building blocks ------------------------------
+wb_status wb_linear(const void* a, const void* w, int M, int N, int K, int dtype, const float* bias,
+                    const float* scale_a, const float* scale_w, int gelu, const void* resid, void* out,
+                    void* stream) {
+  if (M < 0 || N < 32 || N % 32 != 0 || K < 1) return WB_EINVAL;
+  if (dtype != WB_BF16 && dtype != WB_E4M3) return WB_EUNSUPPORTED;
+  const bool fp8 = dtype == WB_E4M3;
+  if ((fp8 && K % 16 != 0) || (!fp8 && K % 8 != 0)) return WB_EINVAL;
+  if (M == 0) return WB_OK;
+  if (!a || !w || !out || !aligned16(a) || !aligned16(w) || !aligned16(out)) return WB_EINVAL;
+  if (resid && !aligned16(resid)) return WB_EINVAL;
+  if (fp8 && (!scale_a || !scale_w)) return WB_EINVAL;
+  GemmParams p = base_params();
+  p.out = out;
+  p.ldo = N;
+  p.bias = bias;
+  p.act_gelu = gelu ? 1 : 0;
+  p.resid = static_cast<const __nv_bfloat16*>(resid);
+  if (fp8) {
+    p.scale_a = scale_a;
+    p.scale_b = scale_w;
+  }
+  return dense_gemm(a, w, M, N, K, fp8, p, static_cast<cudaStream_t>(stream));
+}
+
+wb_status wb_layernorm(const void* x, const void* residual, const float* g, const float* b, int rows, int d,
+                       float eps, void* y, void* total, void* stream) {
+  if (rows < 0 || d < 128 || d > 2048 || d % 128 != 0 || !(eps > 0.0f)) return WB_EINVAL;
+  if (rows == 0) return WB_OK;
+  if (!x || !g || !b || !y || !aligned16(x) || !aligned16(y)) return WB_EINVAL;
+  if ((residual && !aligned16(residual)) || (total && (!residual || !aligned16(total)))) return WB_EINVAL;
+  WB_CUDA(launch_layernorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(residual), g, b,
+                           rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total), nullptr,
+                           static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+size_t wb_attention_workspace_bytes(int batch, int T, int n_heads) {
+  if (batch < 1 || T < 1 || n_heads < 1) return 0;
+  return static_cast<size_t>(batch) * n_heads * 64 * T_PAD * 2;
+}
+
+wb_status wb_attention(const void* q, const void* k, const void* v, int batch, int T, int n_heads, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || T < 1 || T > T_PAD || n_heads < 1 || n_heads > 32) return WB_EINVAL;
+  if (batch == 0) return WB_OK;
+  if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return WB_EINVAL;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < wb_attention_workspace_bytes(batch, T, n_heads))
+    return WB_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto* vt = static_cast<__nv_bfloat16*>(workspace);
+  const long long d = 64LL * n_heads;
+  WB_CUDA(launch_transpose_v(static_cast<const __nv_bfloat16*>(v), d, batch, T, n_heads, vt, s));
+  return run_attention(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), d, vt, batch, T,
+                       n_heads, static_cast<__nv_bfloat16*>(out), s);
+}
+
+}  // extern "C"

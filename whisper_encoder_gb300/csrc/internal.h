@@ -1,0 +1,60 @@
+// Host-side declarations shared by the translation units of libwb.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "types.h"
+
+namespace wb {
+
+constexpr int N_FFT = 400;
+constexpr int HOP = 160;
+constexpr int N_FRAMES = 3000;
+constexpr int CHUNK = 480000;
+constexpr int PAD = N_FFT / 2;
+constexpr int PADDED = CHUNK + 2 * PAD;      // 480400 samples per reflect-padded chunk
+constexpr int DFT_ROWS = 512;                // 2 tiles x (128 cos + 128 sin) basis rows
+constexpr int N_BIN_PAD = 256;               // power-spectrum bins padded 201 -> 256
+constexpr int MEL_ROWS = 128;                // mel filterbank rows padded to one N tile
+constexpr int T_TOK = 1500;                  // encoder positions per chunk
+constexpr int T_PAD = 1504;                  // V^T row length (16-byte aligned rows)
+
+// ---- launchers of the SIMT kernels (kernels.cu) ----
+cudaError_t launch_pad_split(const float* audio, long long n_samples, long long stride, int n_chunks,
+                             __nv_bfloat16* xs, cudaStream_t s);
+cudaError_t launch_dft_basis(__nv_bfloat16* basis, cudaStream_t s);
+cudaError_t launch_mel_fb(__nv_bfloat16* fbs, int n_mels, cudaStream_t s);
+cudaError_t launch_logmel_post(float* out, const float* mel_max, int n_chunks, int n_mels, cudaStream_t s);
+cudaError_t launch_stem_transpose(const float* logmel, int batch, int n_mels, __nv_bfloat16* yTp,
+                                  cudaStream_t s);
+cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16* packed, cudaStream_t s);
+cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
+                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
+                             cudaStream_t s);
+cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaStream_t s);
+cudaError_t launch_quantize(const __nv_bfloat16* x, long long n, uint8_t* q, const float* amax,
+                            float* scale_out, cudaStream_t s);
+cudaError_t launch_finalize_scale(float* amax_to_scale, cudaStream_t s);
+cudaError_t launch_dequantize(const uint8_t* q, const float* scale, long long n, __nv_bfloat16* y,
+                              cudaStream_t s);
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H,
+                               __nv_bfloat16* vt, cudaStream_t s);
+cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long batch_stride_elems,
+                             int batch, int row, cudaStream_t s);
+
+// ---- tensor-core kernels (tc_kernels.cu) ----
+struct GemmLaunch {
+  CUtensorMap amap[GEMM_MAX_AMAPS];
+  CUtensorMap bmap;
+  GemmParams p;
+  int bn;       // 128 or 256
+  bool fp8;
+  int epi;      // EpiKind
+};
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+cudaError_t launch_attention(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt,
+                             const AttnParams& p, cudaStream_t s);
+int sm_count();
+
+}  // namespace wb

@@ -1,0 +1,458 @@
+// Bandwidth-bound SIMT kernels of libwb: audio framing prep, constant tables
+// (DFT basis, mel filterbank), log-mel clamp/scale, conv-stem re-layout,
+// fused residual + LayerNorm, FP8 absmax / quantise / dequantise.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace wb {
+
+namespace {
+
+constexpr int EW_THREADS = 256;
+
+int grid_for(long long work, int per_block, int cap = 152 * 32) {
+  long long g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return static_cast<int>(g);
+}
+
+// ---------------------------------------------------------------------------
+// Reflect-pad each 30 s chunk by 200 samples (mirror without the edge sample)
+// and split every float32 sample exactly into three bf16 parts (hi + mid +
+// lo), the operand of the split-precision DFT.  xs: [n_chunks][3][PADDED].
+// ---------------------------------------------------------------------------
+__global__ void pad_split_kernel(const float* __restrict__ audio, long long n_samples, long long stride,
+                                 int n_chunks, __nv_bfloat16* __restrict__ xs) {
+  const long long total = static_cast<long long>(n_chunks) * PADDED;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i / PADDED);
+    const int j = static_cast<int>(i % PADDED);
+    int src = j - PAD;
+    if (src < 0) src = -src;
+    else if (src >= CHUNK) src = 2 * (CHUNK - 1) - src;
+    const long long g = static_cast<long long>(c) * stride + src;
+    const float x = g < n_samples ? __ldg(audio + g) : 0.0f;
+    const __nv_bfloat16 a = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(a);
+    const __nv_bfloat16 b = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 e = __float2bfloat16_rn(r1 - __bfloat162float(b));
+    __nv_bfloat16* base = xs + static_cast<long long>(c) * 3 * PADDED;
+    base[j] = a;
+    base[PADDED + j] = b;
+    base[2 * PADDED + j] = e;
+  }
+}
+
+// Windowed real-DFT basis, [3 parts][512 rows][400]: rows 256*t + c hold, for
+// tile t, c < 128: w[k] cos(2 pi bin k / 400) and c >= 128: -w[k] sin(...),
+// bin = 128 t + (c mod 128); bins above 200 are zero.  The phase index
+// bin*k mod 400 is reduced exactly in integers; values are formed in double
+// and split into three bf16 parts.
+__global__ void dft_basis_kernel(__nv_bfloat16* __restrict__ basis) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= DFT_ROWS * N_FFT) return;
+  const int row = idx / N_FFT, k = idx % N_FFT;
+  const int tile = row / 256, col = row % 256;
+  const int bin = tile * 128 + (col & 127);
+  double v = 0.0;
+  if (bin <= N_FFT / 2) {
+    const double w = 0.5 - 0.5 * cospi(static_cast<double>(k) / 200.0);
+    const int ph = (bin * k) % N_FFT;
+    double s, c;
+    sincospi(static_cast<double>(ph) / 200.0, &s, &c);
+    v = w * (col >= 128 ? -s : c);
+  }
+  const __nv_bfloat16 a = __double2bfloat16(v);
+  const double r1 = v - static_cast<double>(__bfloat162float(a));
+  const __nv_bfloat16 b = __double2bfloat16(r1);
+  const __nv_bfloat16 e = __double2bfloat16(r1 - static_cast<double>(__bfloat162float(b)));
+  basis[(0 * DFT_ROWS + row) * N_FFT + k] = a;
+  basis[(1 * DFT_ROWS + row) * N_FFT + k] = b;
+  basis[(2 * DFT_ROWS + row) * N_FFT + k] = e;
+}
+
+__device__ double hz_to_mel(double f) {
+  return f < 1000.0 ? 3.0 * f / 200.0 : 15.0 + 27.0 * log(f / 1000.0) / log(6.4);
+}
+__device__ double mel_to_hz(double m) {
+  return m < 15.0 ? 200.0 * m / 3.0 : 1000.0 * exp((m - 15.0) * log(6.4) / 27.0);
+}
+
+// Slaney mel filterbank over 0-8 kHz at the 201 bins of a 400-point DFT,
+// [2 parts][128 rows][256 bins] (rows >= n_mels and bins > 200 are zero):
+// triangle from edge m to edge m+2 peaking at edge m+1, area-normalised by
+// 2 / (edge[m+2] - edge[m]); edges equally spaced on the Slaney mel scale.
+__global__ void mel_fb_kernel(__nv_bfloat16* __restrict__ fbs, int n_mels) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= MEL_ROWS * N_BIN_PAD) return;
+  const int m = idx / N_BIN_PAD, k = idx % N_BIN_PAD;
+  double v = 0.0;
+  if (m < n_mels && k <= N_FFT / 2) {
+    const double step = hz_to_mel(8000.0) / (n_mels + 1);
+    const double lo = mel_to_hz(m * step), ce = mel_to_hz((m + 1) * step), hi = mel_to_hz((m + 2) * step);
+    const double f = 40.0 * k;
+    const double up = (f - lo) / (ce - lo), dn = (hi - f) / (hi - ce);
+    v = fmax(0.0, fmin(up, dn)) * 2.0 / (hi - lo);
+  }
+  const __nv_bfloat16 a = __double2bfloat16(v);
+  const __nv_bfloat16 b = __double2bfloat16(v - static_cast<double>(__bfloat162float(a)));
+  fbs[m * N_BIN_PAD + k] = a;
+  fbs[(MEL_ROWS + m) * N_BIN_PAD + k] = b;
+}
+
+// y = (max(L, log10(max(chunk max, 1e-10)) - 8) + 4) / 4, in place on [n_chunks][n_mels*3000].
+__global__ void logmel_post_kernel(float* __restrict__ out, const float* __restrict__ mel_max, int per_chunk) {
+  const int b = blockIdx.y;
+  const float thr = log10f(fmaxf(mel_max[b], 1e-10f)) - 8.0f;
+  float4* p = reinterpret_cast<float4*>(out + static_cast<long long>(b) * per_chunk);
+  const int n4 = per_chunk / 4;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
+    float4 v = p[i];
+    v.x = (fmaxf(v.x, thr) + 4.0f) * 0.25f;
+    v.y = (fmaxf(v.y, thr) + 4.0f) * 0.25f;
+    v.z = (fmaxf(v.z, thr) + 4.0f) * 0.25f;
+    v.w = (fmaxf(v.w, thr) + 4.0f) * 0.25f;
+    p[i] = v;
+  }
+}
+
+// log-mel [B][C][3000] float32 -> time-major bf16 rows 1..3000 of yTp [B][3002][C].
+__global__ void stem_transpose_kernel(const float* __restrict__ in, int C, __nv_bfloat16* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int b = blockIdx.z, t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
+    const int c = c0 + ty, t = t0 + threadIdx.x;
+    tile[ty][threadIdx.x] = (c < C && t < N_FRAMES) ? in[(static_cast<long long>(b) * C + c) * N_FRAMES + t] : 0.0f;
+  }
+  __syncthreads();
+  for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
+    const int t = t0 + ty, c = c0 + threadIdx.x;
+    if (t < N_FRAMES && c < C)
+      out[(static_cast<long long>(b) * (N_FRAMES + 2) + 1 + t) * C + c] = __float2bfloat16_rn(tile[threadIdx.x][ty]);
+  }
+}
+
+__global__ void zero_rows_kernel(__nv_bfloat16* base, long long row_elems, long long batch_stride, int batch,
+                                 int row) {
+  const int b = blockIdx.y;
+  if (b >= batch) return;
+  __nv_bfloat16* p = base + b * batch_stride + row * row_elems;
+  for (long long i = blockIdx.x * blockDim.x + threadIdx.x; i < row_elems; i += gridDim.x * blockDim.x)
+    p[i] = __float2bfloat16_rn(0.0f);
+}
+
+// PyTorch Conv1d weight [c_out][c_in][3] float32 -> tap-major bf16 [3][c_out][c_in].
+__global__ void pack_conv_kernel(const float* __restrict__ w, int c_out, int c_in, __nv_bfloat16* __restrict__ out) {
+  const long long n = static_cast<long long>(c_out) * c_in * 3;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(i % 3);
+    const long long oi = i / 3;   // o * c_in + ci
+    out[j * static_cast<long long>(c_out) * c_in + oi] = __float2bfloat16_rn(w[i]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused residual + LayerNorm: one warp per row of width NV*VEC*32, the row
+// held in registers (exact two-pass mean / variance), 8- or 16-byte loads.
+// ---------------------------------------------------------------------------
+template <int VEC>
+struct VecIO;
+template <>
+struct VecIO<8> {
+  using T = uint4;
+};
+template <>
+struct VecIO<4> {
+  using T = uint2;
+};
+
+template <int NV, int VEC>
+__global__ void layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
+                                 const float* __restrict__ g, const float* __restrict__ bta, int rows, float eps,
+                                 __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ total,
+                                 float* __restrict__ amax) {
+  constexpr int D = NV * VEC * 32;
+  using V = typename VecIO<VEC>::T;
+  const int lane = threadIdx.x & 31;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  float v[NV * VEC];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int off = (i * 32 + lane) * VEC;
+    V u = *reinterpret_cast<const V*>(x + row * D + off);
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) v[i * VEC + j] = __bfloat162float(h[j]);
+    if (res) {
+      V r = *reinterpret_cast<const V*>(res + row * D + off);
+      const __nv_bfloat16* hr = reinterpret_cast<const __nv_bfloat16*>(&r);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) v[i * VEC + j] += __bfloat162float(hr[j]);
+      if (total) {
+        V o;
+        uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int j = 0; j < VEC / 2; ++j) o32[j] = pack_bf16(v[i * VEC + 2 * j], v[i * VEC + 2 * j + 1]);
+        *reinterpret_cast<V*>(total + row * D + off) = o;
+      }
+    }
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV * VEC; ++i) s += v[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s * (1.0f / D);
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV * VEC; ++i) {
+    const float t = v[i] - mean;
+    q += t * t;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  const float rstd = rsqrtf(q * (1.0f / D) + eps);
+  float mx = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int off = (i * 32 + lane) * VEC;
+    V o;
+    uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) {
+      const float y0 = (v[i * VEC + 2 * j] - mean) * rstd * __ldg(g + off + 2 * j) + __ldg(bta + off + 2 * j);
+      const float y1 =
+          (v[i * VEC + 2 * j + 1] - mean) * rstd * __ldg(g + off + 2 * j + 1) + __ldg(bta + off + 2 * j + 1);
+      o32[j] = pack_bf16(y0, y1);
+      if (amax) {
+        const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&o32[j]);
+        mx = fmaxf(mx, fmaxf(fabsf(__bfloat162float(hv.x)), fabsf(__bfloat162float(hv.y))));
+      }
+    }
+    *reinterpret_cast<V*>(y + row * D + off) = o;
+  }
+  if (amax) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0 && mx > 0.0f) atomic_max_nonneg(amax, mx);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 per-tensor scaling.
+// ---------------------------------------------------------------------------
+__global__ void amax_kernel(const __nv_bfloat16* __restrict__ x, long long n, float* __restrict__ amax) {
+  float m = 0.0f;
+  const long long n8 = n / 8;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = tid; i < n8; i += step) {
+    uint4 u = reinterpret_cast<const uint4*>(x)[i];
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(__bfloat162float(h[j])));
+  }
+  for (long long i = n8 * 8 + tid; i < n; i += step) m = fmaxf(m, fabsf(__bfloat162float(x[i])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wm[32];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? wm[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0 && m > 0.0f) atomic_max_nonneg(amax, m);
+  }
+}
+
+// code = E4M3_rn_satfinite(x * inv), inv = 448 / amax (1 if amax == 0), all float32.
+__global__ void quantize_kernel(const __nv_bfloat16* __restrict__ x, long long n, uint8_t* __restrict__ q,
+                                const float* __restrict__ amax, float* __restrict__ scale_out) {
+  const float a = *amax;
+  const float inv = a > 0.0f ? 448.0f / a : 1.0f;
+  if (scale_out && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = a > 0.0f ? a / 448.0f : 1.0f;
+  const long long n16 = n / 16;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = tid; i < n16; i += step) {
+    const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * i;
+    uint4 u0 = src[0], u1 = src[1];
+    const __nv_bfloat16* h0 = reinterpret_cast<const __nv_bfloat16*>(&u0);
+    const __nv_bfloat16* h1 = reinterpret_cast<const __nv_bfloat16*>(&u1);
+    uint4 o;
+    uint16_t* o16 = reinterpret_cast<uint16_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o16[j] = cvt_e4m3x2(__bfloat162float(h0[2 * j]) * inv, __bfloat162float(h0[2 * j + 1]) * inv);
+      o16[4 + j] = cvt_e4m3x2(__bfloat162float(h1[2 * j]) * inv, __bfloat162float(h1[2 * j + 1]) * inv);
+    }
+    reinterpret_cast<uint4*>(q)[i] = o;
+  }
+  for (long long i = n16 * 16 + tid; i < n; i += step)
+    q[i] = static_cast<uint8_t>(cvt_e4m3x2(__bfloat162float(x[i]) * inv, 0.0f) & 0xFF);
+}
+
+__global__ void finalize_scale_kernel(float* p) {
+  const float a = *p;
+  *p = a > 0.0f ? a / 448.0f : 1.0f;
+}
+
+__global__ void dequantize_kernel(const uint8_t* __restrict__ q, const float* __restrict__ scale, long long n,
+                                  __nv_bfloat16* __restrict__ y) {
+  const float s = *scale;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint16_t two = static_cast<uint16_t>(q[i]);
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    const __half lo = __ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFF));
+    y[i] = __float2bfloat16_rn(__half2float(lo) * s);
+  }
+}
+
+// v [batch*T][ld] (head h at columns 64h..64h+63) -> vt [(b*H + h)*64 + e][T_PAD]
+__global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, long long ld, int T, int H,
+                                   __nv_bfloat16* __restrict__ vt) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const int b = blockIdx.z;
+  const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;  // c over H*64 columns
+  for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
+    const int t = t0 + ty;
+    tile[ty][threadIdx.x] =
+        t < T ? v[(static_cast<long long>(b) * T + t) * ld + c0 + threadIdx.x] : __float2bfloat16_rn(0.0f);
+  }
+  __syncthreads();
+  for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
+    const int c = c0 + ty, t = t0 + threadIdx.x;
+    const int h = c >> 6, e = c & 63;
+    if (t < T) vt[(static_cast<long long>(b * H + h) * 64 + e) * T_PAD + t] = tile[threadIdx.x][ty];
+  }
+}
+
+}  // namespace
+
+// ------------------------------- launchers ---------------------------------
+cudaError_t launch_pad_split(const float* audio, long long n_samples, long long stride, int n_chunks,
+                             __nv_bfloat16* xs, cudaStream_t s) {
+  pad_split_kernel<<<grid_for(static_cast<long long>(n_chunks) * PADDED, EW_THREADS), EW_THREADS, 0, s>>>(
+      audio, n_samples, stride, n_chunks, xs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dft_basis(__nv_bfloat16* basis, cudaStream_t s) {
+  dft_basis_kernel<<<(DFT_ROWS * N_FFT + 255) / 256, 256, 0, s>>>(basis);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mel_fb(__nv_bfloat16* fbs, int n_mels, cudaStream_t s) {
+  mel_fb_kernel<<<(MEL_ROWS * N_BIN_PAD + 255) / 256, 256, 0, s>>>(fbs, n_mels);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logmel_post(float* out, const float* mel_max, int n_chunks, int n_mels, cudaStream_t s) {
+  const int per_chunk = n_mels * N_FRAMES;
+  dim3 grid(grid_for(per_chunk / 4, EW_THREADS, 64), n_chunks);
+  logmel_post_kernel<<<grid, EW_THREADS, 0, s>>>(out, mel_max, per_chunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stem_transpose(const float* logmel, int batch, int n_mels, __nv_bfloat16* yTp,
+                                  cudaStream_t s) {
+  dim3 grid((N_FRAMES + 31) / 32, (n_mels + 31) / 32, batch);
+  stem_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(logmel, n_mels, yTp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_zero_rows(yTp, n_mels, static_cast<long long>(N_FRAMES + 2) * n_mels, batch, 0, s);
+  if (e != cudaSuccess) return e;
+  return launch_zero_rows(yTp, n_mels, static_cast<long long>(N_FRAMES + 2) * n_mels, batch, N_FRAMES + 1, s);
+}
+
+cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long batch_stride_elems, int batch,
+                             int row, cudaStream_t s) {
+  dim3 grid(grid_for(row_elems, EW_THREADS, 16), batch);
+  zero_rows_kernel<<<grid, EW_THREADS, 0, s>>>(base, row_elems, batch_stride_elems, batch, row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16* packed, cudaStream_t s) {
+  pack_conv_kernel<<<grid_for(static_cast<long long>(c_out) * c_in * 3, EW_THREADS), EW_THREADS, 0, s>>>(
+      w, c_out, c_in, packed);
+  return cudaGetLastError();
+}
+
+template <int NV, int VEC>
+static cudaError_t ln_launch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
+                             int rows, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
+                             cudaStream_t s) {
+  const int warps = 8;
+  layernorm_kernel<NV, VEC><<<(rows + warps - 1) / warps, warps * 32, 0, s>>>(x, res, g, b, rows, eps, y, total,
+                                                                               amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
+                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
+                             cudaStream_t s) {
+#define WB_LN_CASE(NV, VEC) \
+  case NV * VEC * 32:       \
+    return ln_launch<NV, VEC>(x, res, g, b, rows, eps, y, total, amax, s);
+  switch (d) {
+    WB_LN_CASE(1, 4)
+    WB_LN_CASE(1, 8)
+    WB_LN_CASE(3, 4)
+    WB_LN_CASE(2, 8)
+    WB_LN_CASE(5, 4)
+    WB_LN_CASE(3, 8)
+    WB_LN_CASE(7, 4)
+    WB_LN_CASE(4, 8)
+    WB_LN_CASE(9, 4)
+    WB_LN_CASE(5, 8)
+    WB_LN_CASE(11, 4)
+    WB_LN_CASE(6, 8)
+    WB_LN_CASE(13, 4)
+    WB_LN_CASE(7, 8)
+    WB_LN_CASE(15, 4)
+    WB_LN_CASE(8, 8)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef WB_LN_CASE
+}
+
+cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaStream_t s) {
+  amax_kernel<<<grid_for(n / 8 + 1, EW_THREADS, 152 * 8), EW_THREADS, 0, s>>>(x, n, amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const __nv_bfloat16* x, long long n, uint8_t* q, const float* amax, float* scale_out,
+                            cudaStream_t s) {
+  quantize_kernel<<<grid_for(n / 16 + 1, EW_THREADS, 152 * 16), EW_THREADS, 0, s>>>(x, n, q, amax, scale_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_scale(float* amax_to_scale, cudaStream_t s) {
+  finalize_scale_kernel<<<1, 1, 0, s>>>(amax_to_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* q, const float* scale, long long n, __nv_bfloat16* y,
+                              cudaStream_t s) {
+  dequantize_kernel<<<grid_for(n, EW_THREADS), EW_THREADS, 0, s>>>(q, scale, n, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H, __nv_bfloat16* vt,
+                               cudaStream_t s) {
+  dim3 grid((T + 31) / 32, H * 2, batch);
+  transpose_v_kernel<<<grid, dim3(32, 8), 0, s>>>(v, ld, T, H, vt);
+  return cudaGetLastError();
+}
+
+}  // namespace wb

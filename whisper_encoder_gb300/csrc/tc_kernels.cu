@@ -1,0 +1,63 @@
+// Instantiation and launch of the tensor-core kernels (GEMM family, attention).
+#include <mutex>
+
+#include "internal.h"
+#include "gemm.cuh"
+#include "attention.cuh"
+
+namespace wb {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+namespace {
+
+template <int BN, bool FP8, int EPI>
+cudaError_t gemm_launch_t(const GemmLaunch& g, cudaStream_t s) {
+  auto kern = gemm_kernel<BN, FP8, EPI>;
+  const int smem = GemmSmem<BN>::TOTAL;
+  // cudaFuncSetAttribute is cheap and idempotent; doing it per call keeps
+  // multi-device processes correct without per-device bookkeeping.
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int m_tiles = (g.p.M + GEMM_BM - 1) / GEMM_BM;
+  const int n_tiles = (g.p.N + BN - 1) / BN;
+  const long long tiles = static_cast<long long>(m_tiles) * n_tiles * g.p.batch;
+  int grid = sm_count();
+  if (tiles < grid) grid = static_cast<int>(tiles);
+  if (grid < 1) return cudaSuccess;
+  kern<<<grid, GEMM_THREADS, smem, s>>>(g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap, g.p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
+  if (g.epi == EPI_STD) {
+    if (g.bn == 256) return g.fp8 ? gemm_launch_t<256, true, EPI_STD>(g, s) : gemm_launch_t<256, false, EPI_STD>(g, s);
+    if (g.bn == 128) return g.fp8 ? gemm_launch_t<128, true, EPI_STD>(g, s) : gemm_launch_t<128, false, EPI_STD>(g, s);
+  } else if (g.epi == EPI_POWER && g.bn == 256 && !g.fp8) {
+    return gemm_launch_t<256, false, EPI_POWER>(g, s);
+  } else if (g.epi == EPI_MEL && g.bn == 128 && !g.fp8) {
+    return gemm_launch_t<128, false, EPI_MEL>(g, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt,
+                             const AttnParams& p, cudaStream_t s) {
+  const int smem = AttnSmem::TOTAL;
+  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (p.T + ATT_BQ - 1) / ATT_BQ;
+  const long long grid = static_cast<long long>(p.batch) * p.H * n_qt;
+  if (grid < 1) return cudaSuccess;
+  attention_kernel<<<static_cast<unsigned>(grid), ATT_THREADS, smem, s>>>(q, k, vt, p);
+  return cudaGetLastError();
+}
+
+}  // namespace wb
