@@ -1,0 +1,413 @@
+#!/usr/bin/env python3
+"""Throughput of the Whisper large-v3 encoder hot path on GB300.
+
+One step = wb_logmel + wb_conv_stem + wb_encoder_forward (32 layers + final
+LayerNorm) over one batch of 32 seeded synthetic 30 s chunks whose audio is
+already resident in device memory.  Metric: audio-seconds processed per
+second (RTFx).  Under torchrun every rank runs an independent replica on its
+own 32 chunks (no data-path collective; weak scaling); the host-side barrier
+and a MAX all-reduce of the elapsed time are the only cross-rank traffic.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--precision bf16|mixed_fp8]
+                    [--batch B] [--impl wb|reference]
+
+--impl reference times the float64 CPU oracle (the reference arm of this
+build) on the host cores, one chunk through log-mel, stem and one encoder
+layer per step, extrapolated to the 32-layer model.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "encoder audio-sec/s (RTFx) at large-v3 batch 32; % of tensor-core peak"
+UNIT = "audio-s/s"
+CHUNK_S = 30.0
+
+
+def flops_per_chunk(dims) -> dict:
+    """Algorithmic FLOPs of one 30 s chunk by kernel class (multiply-add = 2)."""
+    T, d, F, C, H = 1500, dims.d_model, dims.d_ffn, dims.n_mels, dims.n_heads
+    L = dims.n_layers
+    return {
+        "logmel.dft": 2.0 * 3000 * 402 * 400,
+        "logmel.mel": 2.0 * 3000 * C * 201,
+        "stem.conv1": 2.0 * 3000 * d * 3 * C,
+        "stem.conv2": 2.0 * 1500 * d * 3 * d,
+        "enc.qkv": L * 2.0 * T * d * 3 * d,
+        "enc.attention": L * 4.0 * H * T * T * 64,
+        "enc.out_proj": L * 2.0 * T * d * d,
+        "enc.fc1": L * 2.0 * T * d * F,
+        "enc.fc2": L * 2.0 * T * F * d,
+    }
+
+
+def bytes_per_chunk(dims) -> dict:
+    """Algorithmic HBM bytes of the bandwidth-bound classes per chunk."""
+    T, d = 1500, dims.d_model
+    L = dims.n_layers
+    return {"enc.layernorm": (2 * L + 1) * T * d * 2 * 2.0}
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_chunk_seconds(dims, seed: int, n_layers_sample: int = 1) -> tuple[float, dict]:
+    """Time the float64 oracle on one chunk: log-mel, stem, n sample layers, one LN.
+
+    Returns the extrapolated seconds per chunk for the full model and the parts.
+    """
+    from oracle import encoder as oenc
+    from oracle import frontend as ofe
+    w = synthetic.encoder_weights(dims, seed, "bf16", n_layers=n_layers_sample)
+    x = synthetic.tone_chunk(seed)
+    t0 = time.perf_counter()
+    mel = ofe.log_mel(x, dims.n_mels)
+    t1 = time.perf_counter()
+    h = oenc.conv_stem(mel, w)
+    t2 = time.perf_counter()
+    for L in w["layers"]:
+        h = oenc.encoder_layer(h, L, dims.n_heads)
+    t3 = time.perf_counter()
+    oenc.layer_norm(h, w["layers"][0]["ln1_g"], w["layers"][0]["ln1_b"])
+    t4 = time.perf_counter()
+    per_layer = (t3 - t2) / n_layers_sample
+    total = (t1 - t0) + (t2 - t1) + dims.n_layers * per_layer + (t4 - t3)
+    return total, {"logmel_s": t1 - t0, "stem_s": t2 - t1, "layer_s": per_layer, "final_ln_s": t4 - t3}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    dims = synthetic.LARGE_V3
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        t, parts = oracle_chunk_seconds(dims, synthetic.SEED_LARGE_B32 + i % 4)
+        if i >= args.warmup:
+            per_step.append(t)
+    t = statistics.median(per_step)
+    value = CHUNK_S / t
+    sample = ("per step: 1 chunk of 30 s (large-v3 shapes) through the float64 oracle's log-mel, conv stem, "
+              "1 of 32 encoder layers and one LayerNorm; per-chunk time extrapolated as "
+              "logmel + stem + 32 x layer + LN")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000.0, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": arm_config(args, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def replica_seed(base: int, rank: int, batch: int) -> int:
+    """Rank r of an N-replica run encodes its own chunks base + r*batch ... base + r*batch + batch - 1."""
+    return base + rank * batch
+
+
+def job_throughput(local_ms: float, steps: int, batch: int, world: int, reduce_max) -> tuple[float, float]:
+    """Whole-job audio-s/s: every rank's chunks over the slowest rank's time.
+
+    ``reduce_max`` maps this rank's elapsed milliseconds to the maximum over
+    ranks (identity on one process).  Returns (value, ms per step)."""
+    ms_step = reduce_max(local_ms) / steps
+    return world * batch * CHUNK_S / (ms_step / 1000.0), ms_step
+
+
+def workload_name(args) -> str:
+    return (f"whisper large-v3 encoder hot path: log-mel + conv stem + 32 layers + final LN, "
+            f"batch {args.batch} x 30 s synthetic chunks, {args.precision}")
+
+
+def arm_config(args, world: int) -> dict:
+    return {"workload": workload_name(args), "global_batch": world * args.batch, "seq_len": 1500,
+            "parallelism": f"replicas x{world}", "l2": "flushed (256 MB write) between timed steps"}
+
+
+def run_case(args) -> None:
+    """Launch one kernel class at its batch-32 large-v3 shape three times (for ncu captures) and time it."""
+    import torch
+    import whisper_encoder_gb300 as wb
+    wb.load()
+    dims, B = synthetic.LARGE_V3, args.batch
+    M, d, F, H = B * 1500, dims.d_model, dims.d_ffn, dims.n_heads
+    g = torch.Generator(device="cuda").manual_seed(0)
+
+    def rnd(*shape, scale=1.0):
+        return (torch.randn(*shape, device="cuda", generator=g) * scale).to(torch.bfloat16)
+
+    if args.case in ("fc1", "fc2", "qkv", "out"):
+        n, k = {"fc1": (F, d), "fc2": (d, F), "qkv": (3 * d, d), "out": (d, d)}[args.case]
+        a, w = rnd(M, k), rnd(n, k, scale=0.02)
+        bias = torch.zeros(n, device="cuda")
+        fn = lambda: wb.linear(a, w, bias=bias, gelu=args.case == "fc1")  # noqa: E731
+        flops = 2.0 * M * n * k
+    elif args.case == "attention":
+        q, k_, v = rnd(B, 1500, d), rnd(B, 1500, d), rnd(B, 1500, d)
+        fn = lambda: wb.attention(q, k_, v, H)  # noqa: E731
+        flops = 4.0 * B * H * 1500 * 1500 * 64
+    elif args.case == "logmel":
+        audio = torch.randn(B * 480000, device="cuda", generator=g) * 0.1
+        fn = lambda: wb.logmel(audio, B, dims.n_mels)  # noqa: E731
+        flops = B * (2.0 * 3000 * 402 * 400 + 2.0 * 3000 * dims.n_mels * 201)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(3):
+        fn()
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / 3
+    print(json.dumps({"case": args.case, "batch": B, "ms": round(ms, 4),
+                      "tflops": round(flops / (ms / 1000) / 1e12, 1)}))
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--precision", choices=("bf16", "mixed_fp8"), default="bf16")
+    ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "logmel"), default=None,
+                    help="launch one kernel class at full size (for profiler captures) instead of the bench")
+    args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from whisper_encoder_gb300 import build as wbuild
+    if rank == 0 or world == 1:
+        wbuild.build()
+    if dist is not None:
+        dist.barrier()
+    import whisper_encoder_gb300 as wb
+
+    dims = synthetic.LARGE_V3
+    B = args.batch
+    precision = wb.PRESET_BF16 if args.precision == "bf16" else wb.PRESET_MIXED_FP8
+    seed = synthetic.SEED_LARGE_B32
+    host_w = synthetic.encoder_weights(dims, seed, "bf16")
+    stem, enc = wb.upload_weights(host_w)
+    del host_w
+    audio_np = synthetic.tone_batch(replica_seed(seed, rank, B), B).reshape(-1)
+    audio = torch.from_numpy(audio_np).cuda()
+    pipe = wb.Pipeline(dims, stem, enc, B, precision)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        pipe(audio)
+    torch.cuda.synchronize()
+    if wb.check_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")   # > 129 MB L2
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wb.profile_begin()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        pipe(audio)
+        stops[k].record(stream)
+    torch.cuda.synchronize()
+    prof = wb.profile_end()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
+    total_ms = sum(step_ms)
+    if wb.check_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    def reduce_max(v: float) -> float:
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        if dist is not None:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.item()
+
+    value, ms_step = job_throughput(total_ms, args.steps, B, world, reduce_max)
+
+    # ---- end to end: pinned host audio in, encoder output back to pinned host memory, every step
+    audio_host = torch.from_numpy(audio_np).pin_memory()
+    out_host = torch.empty(pipe.out.shape, dtype=pipe.out.dtype).pin_memory()
+    for _ in range(2):
+        audio.copy_(audio_host, non_blocking=True)
+        pipe(audio)
+        out_host.copy_(pipe.out, non_blocking=True)
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        audio.copy_(audio_host, non_blocking=True)
+        pipe(audio)
+        out_host.copy_(pipe.out, non_blocking=True)
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _ = job_throughput(e_start.elapsed_time(e_stop), args.steps, B, world, reduce_max)
+    e2e = {"value": round(e2e_value, 2), "unit": UNIT,
+           "h2d_bytes_per_step": audio_host.numel() * audio_host.element_size(),
+           "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    # ---- roofline of the dominant kernel class, from the events around each launch
+    peaks = load_peaks()
+    fl = flops_per_chunk(dims)
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        per_step_ms = ms / args.steps
+        kernels[name] = {"ms_per_step": round(per_step_ms, 4), "launches_per_step": n // args.steps,
+                         "share": round(ms / max(total_ms, 1e-9), 4)}
+        if name in fl:
+            kernels[name]["tflops"] = round(fl[name] * B / (per_step_ms / 1000.0) / 1e12, 1)
+    fp8_classes = {"enc.qkv", "enc.fc1", "enc.fc2"} if args.precision == "mixed_fp8" else set()
+    tensor_classes = [c for c in prof if c in fl]
+    dom = max(tensor_classes, key=lambda c: prof[c][0])
+    dom_ms, dom_n = prof[dom]
+    per_launch_ms = dom_ms / dom_n
+    flops_launch = fl[dom] * B / (dom_n / args.steps)
+    achieved = flops_launch / (per_launch_ms / 1000.0) / 1e12
+    peak = peaks["bf16_sustained"] * (2.0 if dom in fp8_classes else 1.0)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "flops_per_launch": flops_launch, "ms_per_launch": round(per_launch_ms, 4),
+                "peak_source": f"{peaks['source']} bf16 sustained" + (" x2 (E4M3 nominal ratio)" if dom in fp8_classes else "")}
+    step_flops = sum(fl.values()) * B
+    gpu_launches = sum(n for _, n in prof.values())
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if args.precision == "bf16" else "bf16+e4m3", "data": "synthetic",
+        "impl": "wb",
+        "config": arm_config(args, world),
+        "tflops": round(step_flops / (ms_step / 1000.0) / 1e12, 1),
+        "roofline": roofline, "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks,
+        "kernels": kernels,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, parts = oracle_chunk_seconds(dims, seed)
+        line["cpu_baseline"] = {
+            "value": round(CHUNK_S / t, 5), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": ("1 chunk of 30 s through the float64 oracle's log-mel, conv stem, 1 of 32 layers and one "
+                       "LayerNorm; per-chunk time extrapolated to 32 layers"),
+            "parts_s": {k: round(v, 3) for k, v in parts.items()}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -196,6 +196,17 @@ size_t wb_attention_workspace_bytes(int batch, int T, int n_heads);
 wb_status wb_attention(const void* q, const void* k, const void* v, int batch, int T, int n_heads, void* out,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* --- kernel timing (benchmarks) -------------------------------------------------
+ * Between wb_profile_begin() and wb_profile_end() every kernel that libwb
+ * launches is bracketed by two CUDA events recorded on its launch stream.
+ * wb_profile_end() waits for those events, fills up to max_classes entries
+ * (static class names such as "enc.fc1", summed device milliseconds, and the
+ * number of kernels launched in that class), disables timing and returns the
+ * number of classes.  Any array may be NULL.  Host-side bookkeeping only: use
+ * it from one thread, on one device at a time. */
+wb_status wb_profile_begin(void);
+int wb_profile_end(int max_classes, const char** names, double* total_ms, int64_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

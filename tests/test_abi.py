@@ -1,0 +1,118 @@
+"""CPU checks of the C ABI: libwb builds for sm_103a, loads, exports every
+function include/wb.h declares, and rejects bad arguments on the host before
+touching the GPU.  Also checks that the product path and the oracle share no
+code.  No compute call is made here (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from whisper_encoder_gb300 import build
+    build.build()
+    from whisper_encoder_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "wb.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(wb_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_function_is_exported_and_bound(lib):
+    from whisper_encoder_gb300 import _lib
+    names = declared_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature"
+    assert set(_lib.SIGNATURES) == set(names)
+
+
+def test_status_strings_and_version(lib):
+    from whisper_encoder_gb300 import _lib
+    assert lib.wb_version() >= 100
+    for code, word in [(0, "ok"), (-1, "invalid"), (-4, "timed out"), (-5, "workspace")]:
+        assert word in _lib.status_string(code)
+
+
+def test_workspace_queries_are_host_only(lib):
+    from whisper_encoder_gb300 import _lib
+    import synthetic
+    d = synthetic.LARGE_V3
+    dims = _lib.wb_dims(d.n_mels, d.d_model, d.n_heads, d.n_layers, d.d_ffn)
+    bf = _lib.wb_precision(0, 0, 0, 0, 0, 0)
+    f8 = _lib.wb_precision(1, 1, 0, 0, 1, 1)
+    w_bf = lib.wb_encoder_workspace_bytes(ctypes.byref(dims), 32, ctypes.byref(bf))
+    w_f8 = lib.wb_encoder_workspace_bytes(ctypes.byref(dims), 32, ctypes.byref(f8))
+    M = 32 * 1500
+    assert w_bf >= M * 1280 * 2 * 6 + M * 5120 * 2
+    assert w_f8 >= w_bf + M * 5120          # E4M3 copies of the activations
+    assert lib.wb_logmel_workspace_bytes(32, 128) > 32 * 3 * 480400 * 2
+    assert lib.wb_logmel_workspace_bytes(0, 128) == 0
+    assert lib.wb_conv_stem_workspace_bytes(ctypes.byref(dims), 32) >= 32 * 3001 * 1280 * 2
+    bad = _lib.wb_dims(128, 1000, 20, 32, 5120)                       # d != 64 * heads
+    assert lib.wb_encoder_workspace_bytes(ctypes.byref(bad), 32, ctypes.byref(bf)) == 0
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    from whisper_encoder_gb300 import _lib
+    import synthetic
+    d = synthetic.TINY
+    dims = _lib.wb_dims(d.n_mels, d.d_model, d.n_heads, d.n_layers, d.d_ffn)
+    fake = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced on these paths
+    # log-mel: bad mel count, negative sizes, too-small workspace
+    assert lib.wb_logmel(fake, 480000, 480000, 1, 7, fake, fake, 1 << 30, None) == _lib.WB_EINVAL
+    assert lib.wb_logmel(fake, -1, 480000, 1, 80, fake, fake, 1 << 30, None) == _lib.WB_EINVAL
+    assert lib.wb_logmel(fake, 480000, 480000, 1, 80, fake, fake, 16, None) == _lib.WB_EWORKSPACE
+    assert lib.wb_logmel(None, 480000, 480000, 0, 80, None, None, 0, None) == _lib.WB_OK   # empty batch
+    # encoder: mixed bf16 x E4M3 site, bad layer range, aliasing output, bad dims
+    mixed = _lib.wb_precision(1, 0, 0, 0, 0, 0)
+    assert lib.wb_encoder_forward(fake, 1, ctypes.byref(dims), None, None, ctypes.byref(mixed), 0, 1, 0, fake, fake,
+                                  1 << 30, None) == _lib.WB_EUNSUPPORTED
+    bf = _lib.wb_precision(0, 0, 0, 0, 0, 0)
+    assert lib.wb_encoder_forward(fake, 1, ctypes.byref(dims), None, None, ctypes.byref(bf), 0, 2, 0, fake, fake,
+                                  1 << 30, None) == _lib.WB_EINVAL
+    assert lib.wb_encoder_forward(fake, 1, ctypes.byref(dims), None, None, ctypes.byref(bf), 0, 0, 0, fake, fake,
+                                  1 << 30, None) == _lib.WB_EINVAL
+    bad = _lib.wb_dims(80, 384, 5, 1, 1536)
+    assert lib.wb_encoder_forward(fake, 1, ctypes.byref(bad), None, None, ctypes.byref(bf), 0, 1, 0, fake, fake,
+                                  1 << 30, None) == _lib.WB_EINVAL
+    # linear: N not a multiple of 32, unknown dtype, misaligned pointer, E4M3 without scales
+    assert lib.wb_linear(fake, fake, 16, 33, 64, 0, None, None, None, 0, None, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_linear(fake, fake, 16, 32, 64, 7, None, None, None, 0, None, fake, None) == _lib.WB_EUNSUPPORTED
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.wb_linear(odd, fake, 16, 32, 64, 0, None, None, None, 0, None, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_linear(fake, fake, 16, 32, 64, 1, None, None, None, 0, None, fake, None) == _lib.WB_EINVAL
+    # layernorm: width not a multiple of 128; attention: T beyond the padded V^T rows
+    assert lib.wb_layernorm(fake, None, fake, fake, 4, 200, 1e-5, fake, None, None) == _lib.WB_EINVAL
+    assert lib.wb_attention(fake, fake, fake, 1, 1505, 2, fake, fake, 1 << 30, None) == _lib.WB_EINVAL
+    assert lib.wb_quantize_fp8(fake, -1, fake, fake, None) == _lib.WB_EINVAL
+
+
+def _imports(path):
+    out = []
+    for dirpath, _, files in os.walk(path):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                out += re.findall(r"^\s*(?:from|import)\s+([\w\.]+)", src, flags=re.M)
+                out += re.findall(r'#include\s+"([^"]+)"', src)
+    return out
+
+
+def test_product_and_oracle_share_no_code():
+    prod = _imports(os.path.join(ROOT, "whisper_encoder_gb300"))
+    assert not [m for m in prod if m.startswith("oracle") or "oracle" in m], prod
+    orc = _imports(os.path.join(ROOT, "oracle"))
+    assert not [m for m in orc if "whisper_encoder_gb300" in m or m.startswith("synthetic")], orc
+    # the shared input module holds no step of the method (no FFT, mel, norm or softmax code)
+    src = open(os.path.join(ROOT, "synthetic", "__init__.py")).read()
+    for word in ("fft", "mel_", "log10", "softmax", "layer_norm", "erf"):
+        assert word not in src, word

@@ -62,6 +62,8 @@ SIGNATURES = {
     "wb_layernorm": (c_int, [c_void, c_void, c_void, c_void, c_int, c_int, c_float, c_void, c_void, c_void]),
     "wb_attention_workspace_bytes": (c_size, [c_int, c_int, c_int]),
     "wb_attention": (c_int, [c_void, c_void, c_void, c_int, c_int, c_int, c_void, c_void, c_size, c_void]),
+    "wb_profile_begin": (c_int, []),
+    "wb_profile_end": (c_int, [c_int, P(ctypes.c_char_p), P(ctypes.c_double), P(ctypes.c_int64)]),
 }
 
 _LIB = None

@@ -167,6 +167,21 @@ def attention(q, k, v, n_heads: int, stream=None) -> torch.Tensor:
     return out
 
 
+def profile_begin() -> None:
+    """Start timing every libwb kernel launch (CUDA events on the launch stream)."""
+    call("wb_profile_begin")
+
+
+def profile_end() -> dict:
+    """Stop timing; {kernel class: (summed device ms, kernels launched)}."""
+    n = 32
+    names = (ctypes.c_char_p * n)()
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    k = load().wb_profile_end(n, names, ms, cnt)
+    return {names[i].decode(): (ms[i], cnt[i]) for i in range(min(k, n)) if cnt[i] > 0}
+
+
 def check_device_error(stream=None) -> int:
     word = ctypes.c_uint32(0)
     call("wb_check_device_error", _stream(stream), ctypes.byref(word))

@@ -4,6 +4,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/wb.h"
 #include "internal.h"
@@ -85,6 +86,57 @@ bool b_map(CUtensorMap* m, bool u8, const void* base, uint64_t k, uint64_t n, ui
   return make_map(m, u8, 3, base, dims, str, box);
 }
 
+
+// ------------------------------ kernel timing -------------------------------
+// While enabled, every libwb launch is bracketed by two CUDA events recorded
+// on its own stream; wb_profile_end() sums the elapsed times per kernel class.
+enum ProfClass {
+  PC_LOGMEL_PREP, PC_LOGMEL_DFT, PC_LOGMEL_MEL, PC_LOGMEL_POST, PC_STEM_PREP, PC_STEM_CONV1, PC_STEM_CONV2,
+  PC_ENC_LN, PC_ENC_QUANT, PC_ENC_QKV, PC_ENC_ATTN, PC_ENC_OUT, PC_ENC_FC1, PC_ENC_FC2, PC_OTHER, PC_COUNT
+};
+const char* const kProfNames[PC_COUNT] = {
+    "logmel.prep", "logmel.dft", "logmel.mel", "logmel.post", "stem.prep", "stem.conv1", "stem.conv2",
+    "enc.layernorm", "enc.quantize", "enc.qkv", "enc.attention", "enc.out_proj", "enc.fc1", "enc.fc2", "other"};
+
+struct ProfRec {
+  int cls, kernels;
+  cudaEvent_t a, b;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct Prof {
+  int cls, kernels;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  Prof(int c, cudaStream_t st, int k = 1) : cls(c), kernels(k), s(st) {
+    if (!g_prof_on) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    a = prof_event();
+    if (a) cudaEventRecord(a, s);
+  }
+  ~Prof() {
+    if (!a) return;
+    std::lock_guard<std::mutex> lk(g_mu);
+    cudaEvent_t b = prof_event();
+    if (!b) return;
+    cudaEventRecord(b, s);
+    g_prof_recs.push_back(ProfRec{cls, kernels, a, b});
+  }
+};
+
 // ------------------------------ helpers ------------------------------------
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -116,7 +168,8 @@ void one_pass(GemmParams& p, int n_kb) {
 }
 
 // Plain GEMM out[M, N] = epilogue(A[M, K] . W[N, K]^T), A and W dense row-major.
-wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8, GemmParams p, cudaStream_t s) {
+wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8, GemmParams p, cudaStream_t s,
+                     int prof_cls = PC_OTHER) {
   GemmLaunch g;
   std::memset(&g, 0, sizeof(g));
   const uint64_t es = fp8 ? 1 : 2;
@@ -134,7 +187,10 @@ wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8
   const int bk = fp8 ? 128 : 64;
   one_pass(p, (K + bk - 1) / bk);
   g.p = p;
-  WB_CUDA(launch_gemm(g, s));
+  {
+    Prof pr(prof_cls, s);
+    WB_CUDA(launch_gemm(g, s));
+  }
   return WB_OK;
 }
 
@@ -221,6 +277,7 @@ wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long lon
   p.scale_log2 = 1.4426950408889634f / 8.0f;
   p.out = out;
   p.err = err_ptr();
+  Prof pr(PC_ENC_ATTN, s);
   WB_CUDA(launch_attention(qm, km, vm, p, s));
   return WB_OK;
 }
@@ -282,9 +339,12 @@ wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride,
   auto* mmax = reinterpret_cast<float*>(ws + L.mmax);
 
   WB_CUDA(cudaMemsetAsync(mmax, 0, n_chunks * sizeof(float), s));
-  WB_CUDA(launch_dft_basis(basis, s));
-  WB_CUDA(launch_mel_fb(fbs, n_mels, s));
-  WB_CUDA(launch_pad_split(audio, n_samples, chunk_stride, n_chunks, xs, s));
+  {
+    Prof pr(PC_LOGMEL_PREP, s, 3);
+    WB_CUDA(launch_dft_basis(basis, s));
+    WB_CUDA(launch_mel_fb(fbs, n_mels, s));
+    WB_CUDA(launch_pad_split(audio, n_samples, chunk_stride, n_chunks, xs, s));
+  }
 
   // Windowed DFT: frames are read as four column segments of the padded
   // signal (row t starts at sample 160 t), each times its slice of the basis,
@@ -317,6 +377,7 @@ wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride,
     p.pw = pw;
     p.pw_ld = N_BIN_PAD;
     g.p = p;
+    Prof pr(PC_LOGMEL_DFT, s);
     WB_CUDA(launch_gemm(g, s));
   }
   // Mel filterbank: power (hi, lo) x filterbank (hi, lo), three leading products.
@@ -346,9 +407,13 @@ wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride,
     p.mel_max = mmax;
     p.n_valid = n_mels;
     g.p = p;
+    Prof pr(PC_LOGMEL_MEL, s);
     WB_CUDA(launch_gemm(g, s));
   }
-  WB_CUDA(launch_logmel_post(out, mmax, n_chunks, n_mels, s));
+  {
+    Prof pr(PC_LOGMEL_POST, s);
+    WB_CUDA(launch_logmel_post(out, mmax, n_chunks, n_mels, s));
+  }
   return WB_OK;
 }
 
@@ -380,8 +445,11 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
   const int C = dims->n_mels, D = dims->d_model;
   const int bn = (D % 256 == 0) ? 256 : 128;
 
-  WB_CUDA(launch_stem_transpose(logmel, batch, C, yTp, s));
-  WB_CUDA(launch_zero_rows(y1p, D, static_cast<long long>(N_FRAMES + 1) * D, batch, 0, s));
+  {
+    Prof pr(PC_STEM_PREP, s, 4);
+    WB_CUDA(launch_stem_transpose(logmel, batch, C, yTp, s));
+    WB_CUDA(launch_zero_rows(y1p, D, static_cast<long long>(N_FRAMES + 1) * D, batch, 0, s));
+  }
   {  // conv1: three taps = three passes over row-shifted views of yTp
     GemmLaunch g;
     std::memset(&g, 0, sizeof(g));
@@ -406,6 +474,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     p.bias = w->conv1_b;
     p.act_gelu = 1;
     g.p = p;
+    Prof pr(PC_STEM_CONV1, s);
     WB_CUDA(launch_gemm(g, s));
   }
   {  // conv2: stride 2 -> one tensor map per tap over every other row of y1p
@@ -436,6 +505,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     p.act_gelu = 1;
     p.add_pe = 1;
     g.p = p;
+    Prof pr(PC_STEM_CONV2, s);
     WB_CUDA(launch_gemm(g, s));
   }
   return WB_OK;
@@ -503,8 +573,14 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     const bool q8 = pr.qkv_a == WB_E4M3, o8 = pr.out_a == WB_E4M3, f8 = pr.ffn_a == WB_E4M3;
 
     // LN1 -> a  [-> E4M3]
-    WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? sl + 0 : nullptr, s));
-    if (q8) WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 0, sl + 1, s));
+    {
+      Prof pr(PC_ENC_LN, s);
+      WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? sl + 0 : nullptr, s));
+    }
+    if (q8) {
+      Prof pr(PC_ENC_QUANT, s);
+      WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 0, sl + 1, s));
+    }
     {  // QKV projection: q | k to qk [M, 2D], v transposed to vt
       GemmParams p = base_params();
       p.out = qk;
@@ -519,7 +595,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.scale_a = sl + 1;
         p.scale_b = W.s_qkv;
       }
-      wb_status st = dense_gemm(q8 ? static_cast<const void*>(aq) : a, W.w_qkv, M, 3 * D, D, q8, p, s);
+      wb_status st = dense_gemm(q8 ? static_cast<const void*>(aq) : a, W.w_qkv, M, 3 * D, D, q8, p, s, PC_ENC_QKV);
       if (st != WB_OK) return st;
     }
     {
@@ -527,6 +603,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
       if (st != WB_OK) return st;
     }
     if (o8) {
+      Prof pr(PC_ENC_QUANT, s, 2);
       WB_CUDA(launch_amax(o, static_cast<long long>(M) * D, sl + 2, s));
       WB_CUDA(launch_quantize(o, static_cast<long long>(M) * D, aq, sl + 2, sl + 3, s));
     }
@@ -540,12 +617,18 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.scale_a = sl + 3;
         p.scale_b = W.s_out;
       }
-      wb_status st = dense_gemm(o8 ? static_cast<const void*>(aq) : o, W.w_out, M, D, D, o8, p, s);
+      wb_status st = dense_gemm(o8 ? static_cast<const void*>(aq) : o, W.w_out, M, D, D, o8, p, s, PC_ENC_OUT);
       if (st != WB_OK) return st;
     }
     // LN2 -> a [-> E4M3]
-    WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? sl + 4 : nullptr, s));
-    if (f8) WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 4, sl + 5, s));
+    {
+      Prof pr(PC_ENC_LN, s);
+      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? sl + 4 : nullptr, s));
+    }
+    if (f8) {
+      Prof pr(PC_ENC_QUANT, s);
+      WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 4, sl + 5, s));
+    }
     {  // FC1 + bias + GELU -> g
       GemmParams p = base_params();
       p.out = g;
@@ -557,10 +640,13 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.scale_b = W.s_fc1;
         p.amax = sl + 6;
       }
-      wb_status st = dense_gemm(f8 ? static_cast<const void*>(aq) : a, W.w_fc1, M, F, D, f8, p, s);
+      wb_status st = dense_gemm(f8 ? static_cast<const void*>(aq) : a, W.w_fc1, M, F, D, f8, p, s, PC_ENC_FC1);
       if (st != WB_OK) return st;
     }
-    if (f8) WB_CUDA(launch_quantize(g, static_cast<long long>(M) * F, gq, sl + 6, sl + 7, s));
+    if (f8) {
+      Prof pr(PC_ENC_QUANT, s);
+      WB_CUDA(launch_quantize(g, static_cast<long long>(M) * F, gq, sl + 6, sl + 7, s));
+    }
     {  // FC2 + bias + residual -> h (or straight to out after the last layer without final LN)
       GemmParams p = base_params();
       p.out = (last && !apply_final_ln) ? outb : h;
@@ -571,12 +657,13 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.scale_a = sl + 7;
         p.scale_b = W.s_fc2;
       }
-      wb_status st = dense_gemm(f8 ? static_cast<const void*>(gq) : g, W.w_fc2, M, D, F, f8, p, s);
+      wb_status st = dense_gemm(f8 ? static_cast<const void*>(gq) : g, W.w_fc2, M, D, F, f8, p, s, PC_ENC_FC2);
       if (st != WB_OK) return st;
     }
   }
   const __nv_bfloat16* final_src = n_layers_run > 0 ? h : x0b;
   if (apply_final_ln) {
+    Prof pr(PC_ENC_LN, s);
     WB_CUDA(launch_layernorm(final_src, nullptr, ln_post->g, ln_post->b, M, D, eps, outb, nullptr, nullptr, s));
   } else if (n_layers_run == 0) {
     WB_CUDA(cudaMemcpyAsync(outb, x0b, static_cast<size_t>(M) * D * 2, cudaMemcpyDeviceToDevice, s));
@@ -662,6 +749,40 @@ wb_status wb_attention(const void* q, const void* k, const void* v, int batch, i
   WB_CUDA(launch_transpose_v(static_cast<const __nv_bfloat16*>(v), d, batch, T, n_heads, vt, s));
   return run_attention(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), d, vt, batch, T,
                        n_heads, static_cast<__nv_bfloat16*>(out), s);
+}
+
+// -------------------------------- profiling ----------------------------------
+wb_status wb_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& r : g_prof_recs) {
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  g_prof_on = true;
+  return WB_OK;
+}
+
+int wb_profile_end(int max_classes, const char** names, double* total_ms, int64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof_on = false;
+  double ms[PC_COUNT] = {0};
+  int64_t cnt[PC_COUNT] = {0};
+  for (auto& r : g_prof_recs) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) ms[r.cls] += t;
+    cnt[r.cls] += r.kernels;
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  const int n = max_classes < PC_COUNT ? max_classes : PC_COUNT;
+  for (int i = 0; i < n; ++i) {
+    if (names) names[i] = kProfNames[i];
+    if (total_ms) total_ms[i] = ms[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return PC_COUNT;
 }
 
 }  // extern "C"
