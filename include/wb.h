@@ -148,11 +148,12 @@ wb_status wb_pack_conv_weight(const float* w, int c_out, int c_in, void* packed,
  * (ln_post); writes bf16 [batch, 1500, d] to `out` (which must not alias x0).
  * Per layer: h += OutProj(Attn(QKV(LN1(h)))); h += FC2(GELU(FC1(LN2(h)))),
  * LayerNorm eps 1e-5 (PyPI page, "Direct Kernel API"), softmax attention over
- * all 1500 positions with scale 1/8, exact-erf GELU.  `precision` selects the
- * operand type of each site; an E4M3 activation is quantised on the device
- * with one per-tensor absmax scale over the whole [batch*1500, k] operand of
- * the call (showcase site, "Learnings": scales from activation maxima).
- * layers[i] is read only for begin <= i < end. */
+ * all 1500 positions with scale 1/8, erf GELU.  `precision` selects the
+ * operand type of each site.  An E4M3 activation is quantised on the device
+ * with an absmax scale per tensor (showcase site, "Learnings": scales from
+ * activation maxima), the tensor being one 30 s chunk's [1500, k] operand:
+ * every chunk gets its own scale, so a chunk's result does not depend on the
+ * other chunks of the batch.  layers[i] is read only for begin <= i < end. */
 size_t wb_encoder_workspace_bytes(const wb_dims* dims, int batch, const wb_precision* precision);
 wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, const wb_layer_weights* layers,
                              const wb_ln_weights* ln_post, const wb_precision* precision, int layer_begin,

@@ -100,31 +100,62 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int) -> np.n
     return out
 
 
-def encoder_layer(h: np.ndarray, L: dict, n_heads: int) -> np.ndarray:
-    """One pre-LN Whisper encoder layer on a [T, d] float64 residual stream."""
+def encoder_layer(h: np.ndarray, L: dict, n_heads: int, fp8_sites=()) -> np.ndarray:
+    """One pre-LN Whisper encoder layer on a [T, d] float64 residual stream.
+
+    ``fp8_sites`` names the layer sites ("qkv", "out", "ffn") whose GEMMs take
+    E4M3 operands (the whisper-blaze showcase site, "The Approach": mixed_fp8
+    puts encoder_attn_qkv and encoder_ffn in E4M3 for weights and activations,
+    encoder_attn_out stays 16-bit).  Each operand then carries one per-tensor
+    absmax scale: the fused [3d, d] QKV weight, W1, W2 and W_o as matrices, and
+    each activation over the whole [T, k] operand after it is stored as bf16.
+    Everything else stays float64.
+    """
+    from . import fp8 as q8
     f64 = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    act = (lambda a: q8.fake_quantize(q8.round_bf16(a)))  # noqa: E731
+    wgt = q8.fake_quantize
+    d = h.shape[1]
     a = layer_norm(h, L["ln1_g"], L["ln1_b"])
-    q = a @ f64(L["wq"]).T + f64(L["bq"])
-    k = a @ f64(L["wk"]).T
-    v = a @ f64(L["wv"]).T + f64(L["bv"])
-    h = h + attention(q, k, v, n_heads) @ f64(L["wo"]).T + f64(L["bo"])
+    w_qkv = np.concatenate([f64(L["wq"]), f64(L["wk"]), f64(L["wv"])])
+    if "qkv" in fp8_sites:
+        qkv = act(a) @ wgt(w_qkv).T
+    else:
+        qkv = a @ w_qkv.T
+    q = qkv[:, :d] + f64(L["bq"])
+    k = qkv[:, d:2 * d]
+    v = qkv[:, 2 * d:] + f64(L["bv"])
+    o = attention(q, k, v, n_heads)
+    if "out" in fp8_sites:
+        h = h + act(o) @ wgt(L["wo"]).T + f64(L["bo"])
+    else:
+        h = h + o @ f64(L["wo"]).T + f64(L["bo"])
     f = layer_norm(h, L["ln2_g"], L["ln2_b"])
-    h = h + gelu(f @ f64(L["w1"]).T + f64(L["b1"])) @ f64(L["w2"]).T + f64(L["b2"])
+    if "ffn" in fp8_sites:
+        g = gelu(act(f) @ wgt(L["w1"]).T + f64(L["b1"]))
+        h = h + act(g) @ wgt(L["w2"]).T + f64(L["b2"])
+    else:
+        h = h + gelu(f @ f64(L["w1"]).T + f64(L["b1"])) @ f64(L["w2"]).T + f64(L["b2"])
     return h
 
 
+MIXED_FP8 = ("qkv", "ffn")
+
+
 def encoder(x0: np.ndarray, weights: dict, n_heads: int, layer_begin: int = 0,
-            layer_end: int | None = None, final_ln: bool = True, capture: list | None = None):
+            layer_end: int | None = None, final_ln: bool = True, capture: list | None = None,
+            fp8_sites=()):
     """Layers [layer_begin, layer_end) on x0 [T, d], then optionally LN_post.
 
     If ``capture`` is a list, the residual stream after every layer is appended.
+    ``fp8_sites`` as in encoder_layer (MIXED_FP8 for the mixed_fp8 preset).
     """
     layers = weights["layers"]
     if layer_end is None:
         layer_end = len(layers)
     h = np.asarray(x0, dtype=np.float64)
     for i in range(layer_begin, layer_end):
-        h = encoder_layer(h, layers[i], n_heads)
+        h = encoder_layer(h, layers[i], n_heads, fp8_sites)
         if capture is not None:
             capture.append(h)
     if final_ln:

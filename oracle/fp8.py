@@ -76,3 +76,21 @@ def quantize(x):
 
 def dequantize(codes, scale) -> np.ndarray:
     return e4m3_decode(codes) * np.float64(scale)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round to bfloat16 (nearest, ties to even) and return the values as float64.
+
+    An activation is stored as bf16 before it is quantised, so the quantisation
+    decision is taken on the bf16 value (the precision the GPU path stores).
+    """
+    x32 = np.ascontiguousarray(x, dtype=np.float32)
+    u = x32.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def fake_quantize(x) -> np.ndarray:
+    """dequantize(quantize(x)): the value an E4M3 operand with one per-tensor scale carries."""
+    codes, scale = quantize(np.asarray(x, dtype=np.float32))
+    return dequantize(codes, scale)

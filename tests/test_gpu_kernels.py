@@ -139,3 +139,25 @@ def test_attention_peaked_scores(wb):
 
 def test_device_error_word_clear(wb):
     assert wb.check_device_error() == 0
+
+
+def test_gelu_epilogue_within_the_erfc_approximation_bound(wb):
+    # zero operands: the FC1 epilogue returns GELU(bias) for a sweep of 4096 bias values.
+    # The epilogue evaluates erfc by Abramowitz & Stegun 7.1.26 (|erf error| <= 1.5e-7), so
+    # |GELU error| <= |x| * 0.75e-7 before the result is rounded to bf16 (half an ulp).
+    N = 4096
+    x = np.concatenate([np.linspace(-8, 8, N - 8), [0.0, 1e-3, -1e-3, 5.5, -5.5, 30.0, -30.0, 2.0]])
+    bias = x.astype(np.float32)
+    a = torch.zeros((64, 64), dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros((N, 64), dtype=torch.bfloat16, device=DEV)
+    got = to_np(wb.linear(a, w, bias=_f32(bias), gelu=True))
+    assert np.all(got == got[0:1])                                   # every row identical
+    g = got[0]
+    exact = oenc.gelu(bias.astype(np.float64))
+    half_ulp = np.where(g != 0, 2.0 ** (np.floor(np.log2(np.abs(np.where(g != 0, g, 1.0)))) - 8), 0.0)
+    bound = half_ulp + 0.75e-7 * np.abs(bias) * 1.001 + 2.0 ** -21 * np.abs(exact) + 1e-30
+    assert np.all(np.abs(g - exact) <= bound), float(np.max(np.abs(g - exact) - bound))
+    # away from the tail the result is the correctly rounded bf16 value or its neighbour
+    ref = synthetic.round_to(exact.astype(np.float32), "bf16").astype(np.float64)
+    body = np.abs(bias) <= 3
+    assert np.all(np.abs(g - ref)[body] <= 2 * half_ulp[body] + 1e-30)

@@ -81,14 +81,16 @@ def test_tiny_pipeline_matches_oracle(wb):
 
 
 def test_tiny_mixed_fp8(wb):
+    # mixed_fp8 against the oracle of the same pipeline (E4M3 operands at the qkv and ffn sites)
     dims, w = _tiny()
     _, enc = wb.upload_weights(w)
     x0 = oenc.conv_stem(ofe.log_mel(synthetic.tone_chunk(5), dims.n_mels), w)
     x0d = _dev(x0[None]).to(torch.bfloat16)
     enc.quantize()
     out = to_np(wb.encoder_forward(x0d, dims, enc, precision=wb.PRESET_MIXED_FP8))[0]
-    ref = oenc.encoder(to_np(x0d)[0], w, dims.n_heads)
-    assert rel_l2(out, ref) < FP8_TOL
+    ref8 = oenc.encoder(to_np(x0d)[0], w, dims.n_heads, fp8_sites=oenc.MIXED_FP8)
+    assert rel_l2(out, ref8) < FP8_TOL
+    assert rel_l2(out, oenc.encoder(to_np(x0d)[0], w, dims.n_heads)) < 0.1
 
 
 def test_encoder_zero_layers_and_range(wb):

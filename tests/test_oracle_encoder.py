@@ -9,6 +9,7 @@ import pytest
 import torch
 
 from oracle import encoder as enc
+oenc = enc
 import synthetic
 
 GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_facts.json")))
@@ -210,3 +211,46 @@ def test_encoder_capture_and_layer_range():
     h1 = enc.encoder(x0, w, dims.n_heads, 0, 1, final_ln=False)
     np.testing.assert_array_equal(h1, cap[0])
     np.testing.assert_array_equal(enc.encoder(h1, w, dims.n_heads, 1, 2), out)
+
+
+def _grid_layer(rng, d, F, beta_on_grid=True):
+    """A layer whose quantised operands all sit exactly on their per-tensor E4M3 grid."""
+    from oracle import fp8 as q8
+    grid = q8.e4m3_decode(np.arange(0x00, 0x7F))                 # non-negative E4M3 values
+    pick = lambda shape, s: (rng.choice(grid[grid <= 448], size=shape) *        # noqa: E731
+                             rng.choice([-1.0, 1.0], size=shape)) * s
+    def with_amax(w):                                              # force amax == 448 * s exactly
+        w = w.copy(); w.flat[0] = 448.0 * (2.0 ** -12); return w
+    L = {"ln1_g": np.zeros(d), "ln2_g": np.zeros(d)}
+    L["ln1_b"] = with_amax(pick(d, 2.0 ** -12)) if beta_on_grid else rng.normal(size=d) * 0.05
+    L["ln2_b"] = with_amax(pick(d, 2.0 ** -12))
+    for k in ("wq", "wk", "wv"):
+        L[k] = pick((d, d), 2.0 ** -14)
+    L["wq"].flat[0] = 448.0 * 2.0 ** -14                           # fused QKV amax on the grid
+    L["wo"] = rng.normal(size=(d, d)) * 0.02
+    L["bq"], L["bv"], L["bo"] = (rng.normal(size=d) * 0.02 for _ in range(3))
+    L["w1"], L["b1"] = np.zeros((F, d)), np.zeros(F)               # GELU(0) = 0: FC2 input exact
+    L["w2"], L["b2"] = pick((d, F), 2.0 ** -14), rng.normal(size=d) * 0.02
+    return L
+
+
+def test_fp8_sites_are_exact_when_operands_sit_on_the_e4m3_grid():
+    rng = np.random.default_rng(8)
+    d, F, H = 128, 256, 2
+    L = _grid_layer(rng, d, F)
+    h = rng.normal(size=(40, d))
+    ref = oenc.encoder_layer(h, L, H)
+    np.testing.assert_allclose(oenc.encoder_layer(h, L, H, oenc.MIXED_FP8), ref, atol=1e-12)
+    np.testing.assert_allclose(oenc.encoder_layer(h, L, H, ("qkv", "out", "ffn")) - ref,
+                               oenc.encoder_layer(h, L, H, ("out",)) - ref, atol=1e-12)
+
+
+def test_fp8_sites_quantise_off_grid_operands():
+    rng = np.random.default_rng(9)
+    d, F, H = 128, 256, 2
+    L = _grid_layer(rng, d, F, beta_on_grid=False)
+    h = rng.normal(size=(40, d))
+    ref = oenc.encoder_layer(h, L, H)
+    diff = np.abs(oenc.encoder_layer(h, L, H, ("qkv",)) - ref).max()
+    assert 1e-6 < diff < 0.1 * np.abs(ref).max()                   # the QKV input was rounded
+    assert np.abs(oenc.encoder_layer(h, L, H, ("ffn",)) - ref).max() < 1e-12   # FC1 input on grid, FC2 input 0

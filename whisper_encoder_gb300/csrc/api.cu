@@ -50,7 +50,7 @@ bool encoder_fn() {
 
 // rank-dimensional tiled map; strides in bytes for dims 1..rank-1; 128-byte swizzle.
 bool make_map(CUtensorMap* m, bool u8, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
-              const uint32_t* box) {
+              const uint32_t* box, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   if (!encoder_fn()) return false;
   cuuint64_t gd[5];
   cuuint64_t gs[4];
@@ -63,7 +63,7 @@ bool make_map(CUtensorMap* m, bool u8, int rank, const void* base, const uint64_
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
   CUresult r = g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -86,6 +86,16 @@ bool b_map(CUtensorMap* m, bool u8, const void* base, uint64_t k, uint64_t n, ui
   return make_map(m, u8, 3, base, dims, str, box);
 }
 
+
+// Output / residual view for the standard epilogues: (n, row, item) with 32 x 32 boxes and the
+// 64-byte swizzle the epilogue writes its staging boxes in.
+bool o_map(CUtensorMap* m, const void* base, uint64_t n, uint64_t rows, uint64_t items, uint64_t ld_elems,
+           uint64_t item_elems) {
+  const uint64_t dims[3] = {n, rows, items};
+  const uint64_t str[2] = {ld_elems * 2, item_elems * 2};
+  const uint32_t box[3] = {32u, 32u, 1u};
+  return make_map(m, false, 3, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
 
 // ------------------------------ kernel timing -------------------------------
 // While enabled, every libwb launch is bracketed by two CUDA events recorded
@@ -158,6 +168,7 @@ GemmParams base_params() {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.batch = 1;
+  p.rows_per_item = T_TOK;
   p.err = err_ptr();
   return p;
 }
@@ -167,20 +178,24 @@ void one_pass(GemmParams& p, int n_kb) {
   p.pass[0] = GemmPass{0, 0, 0, 0, 0, 0, static_cast<int16_t>(n_kb), 0};
 }
 
-// Plain GEMM out[M, N] = epilogue(A[M, K] . W[N, K]^T), A and W dense row-major.
-wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8, GemmParams p, cudaStream_t s,
-                     int prof_cls = PC_OTHER) {
+// Plain GEMM out[M, N] = epilogue(A[M, K] . W[N, K]^T), A and W dense row-major; the output
+// (and residual) rows are ldo elements apart, and the output map covers its first n_store columns.
+wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8, int epi, void* out, long long ldo,
+                     int n_store, const void* resid, GemmParams p, cudaStream_t s, int prof_cls = PC_OTHER) {
   GemmLaunch g;
   std::memset(&g, 0, sizeof(g));
   const uint64_t es = fp8 ? 1 : 2;
   g.bn = (N % 256 == 0 || N > 512) ? 256 : 128;
   g.fp8 = fp8;
-  g.epi = EPI_STD;
+  g.epi = epi;
   if (!a_map(&g.amap[0], fp8, A, K, M, 1, 1, K * es, static_cast<uint64_t>(M) * K * es,
              static_cast<uint64_t>(M) * K * es))
     return WB_ECUDA;
   g.amap[1] = g.amap[2] = g.amap[3] = g.amap[0];
   if (!b_map(&g.bmap, fp8, W, K, N, 1, K * es, static_cast<uint64_t>(N) * K * es, g.bn)) return WB_ECUDA;
+  if (!o_map(&g.omap, out, n_store, M, 1, ldo, static_cast<uint64_t>(M) * ldo)) return WB_ECUDA;
+  g.rmap = g.omap;
+  if (resid && !o_map(&g.rmap, resid, N, M, 1, ldo, static_cast<uint64_t>(M) * ldo)) return WB_ECUDA;
   p.M = M;
   p.N = N;
   p.batch = 1;
@@ -221,7 +236,8 @@ EncLayout enc_layout(const wb_dims* d, int batch, const wb_precision* pr) {
   L.g = c.take(M * F * 2);
   L.aq = any8 ? c.take(M * D) : 0;
   L.gq = ffn8 ? c.take(M * F) : 0;
-  L.slots = c.take(static_cast<size_t>(8) * (d->n_layers > 0 ? d->n_layers : 1) * sizeof(float));
+  // per layer, per E4M3 operand site (qkv, out, fc1, fc2 inputs), per batch item: one absmax
+  L.slots = c.take(static_cast<size_t>(4) * (d->n_layers > 0 ? d->n_layers : 1) * batch * sizeof(float));
   L.total = c.off;
   return L;
 }
@@ -454,7 +470,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     GemmLaunch g;
     std::memset(&g, 0, sizeof(g));
     g.bn = bn;
-    g.epi = EPI_STD;
+    g.epi = EPI_BIAS_GELU;
     const uint64_t rs = static_cast<uint64_t>(C) * 2, item = static_cast<uint64_t>(N_FRAMES + 2) * C * 2;
     if (!a_map(&g.amap[0], false, yTp, C, N_FRAMES + 2, 1, batch, rs, item, item)) return WB_ECUDA;
     g.amap[1] = g.amap[2] = g.amap[3] = g.amap[0];
@@ -467,12 +483,11 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
       p.pass[j] = GemmPass{0, 0, static_cast<int8_t>(j), static_cast<int8_t>(j), 0, 0,
                            static_cast<int16_t>((C + 63) / 64), 0};
     p.n_pass = 3;
-    p.out = y1p;
-    p.ldo = D;
-    p.out_batch_rows = N_FRAMES + 1;
+    // y1 rows go to rows 1..3000 of each item of y1p [batch][3001][D] (row 0 is the zero pad)
+    if (!o_map(&g.omap, y1p, D, N_FRAMES + 1, batch, D, static_cast<uint64_t>(N_FRAMES + 1) * D)) return WB_ECUDA;
+    g.rmap = g.omap;
     p.out_row_off = 1;
     p.bias = w->conv1_b;
-    p.act_gelu = 1;
     g.p = p;
     Prof pr(PC_STEM_CONV1, s);
     WB_CUDA(launch_gemm(g, s));
@@ -481,7 +496,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     GemmLaunch g;
     std::memset(&g, 0, sizeof(g));
     g.bn = bn;
-    g.epi = EPI_STD;
+    g.epi = EPI_CONV2;
     const uint64_t rs = static_cast<uint64_t>(2 * D) * 2;
     for (int j = 0; j < 3; ++j)
       if (!a_map(&g.amap[j], false, y1p + static_cast<long long>(j) * D, D, T_TOK, 1, batch, rs, rs * T_TOK,
@@ -498,12 +513,9 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     for (int j = 0; j < 3; ++j)
       p.pass[j] = GemmPass{static_cast<int8_t>(j), 0, 0, static_cast<int8_t>(j), 0, 0, static_cast<int16_t>(D / 64), 0};
     p.n_pass = 3;
-    p.out = x0;
-    p.ldo = D;
-    p.out_batch_rows = T_TOK;
+    if (!o_map(&g.omap, x0, D, T_TOK, batch, D, static_cast<uint64_t>(T_TOK) * D)) return WB_ECUDA;
+    g.rmap = g.omap;
     p.bias = w->conv2_b;
-    p.act_gelu = 1;
-    p.add_pe = 1;
     g.p = p;
     Prof pr(PC_STEM_CONV2, s);
     WB_CUDA(launch_gemm(g, s));
@@ -563,11 +575,16 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
   const float eps = 1e-5f;
   const int n_layers_run = layer_end - layer_begin;
 
-  if (n_layers_run > 0) WB_CUDA(cudaMemsetAsync(slots, 0, sizeof(float) * 8 * dims->n_layers, s));
+  if (n_layers_run > 0 && (pr.qkv_a == WB_E4M3 || pr.out_a == WB_E4M3 || pr.ffn_a == WB_E4M3))
+    WB_CUDA(cudaMemsetAsync(slots, 0, sizeof(float) * 4 * dims->n_layers * batch, s));
 
   for (int l = layer_begin; l < layer_end; ++l) {
     const wb_layer_weights& W = layers[l];
-    float* sl = slots + 8 * l;  // [qkv amax, qkv scale, out amax, out scale, fc1 amax, fc1 scale, fc2 amax, fc2 scale]
+    // per-item absmax of the E4M3 operands: each 30 s chunk's activation gets its own scale
+    float* am_qkv = slots + (4 * l + 0) * batch;
+    float* am_out = slots + (4 * l + 1) * batch;
+    float* am_fc1 = slots + (4 * l + 2) * batch;
+    float* am_fc2 = slots + (4 * l + 3) * batch;
     const __nv_bfloat16* src = (l == layer_begin) ? x0b : h;
     const bool last = (l == layer_end - 1);
     const bool q8 = pr.qkv_a == WB_E4M3, o8 = pr.out_a == WB_E4M3, f8 = pr.ffn_a == WB_E4M3;
@@ -575,27 +592,25 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     // LN1 -> a  [-> E4M3]
     {
       Prof pr(PC_ENC_LN, s);
-      WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? sl + 0 : nullptr, s));
+      WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? am_qkv : nullptr, T_TOK, s));
     }
     if (q8) {
       Prof pr(PC_ENC_QUANT, s);
-      WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 0, sl + 1, s));
+      WB_CUDA(launch_quantize_rows(a, static_cast<long long>(M) * D, D, T_TOK, am_qkv, aq, s));
     }
     {  // QKV projection: q | k to qk [M, 2D], v transposed to vt
       GemmParams p = base_params();
-      p.out = qk;
-      p.ldo = 2 * D;
-      p.out_batch_rows = 0;
       p.bias = W.b_qkv;
       p.vt = vt;
       p.vt_col0 = 2 * D;
       p.vt_T = T_TOK;
       p.vt_ld = T_PAD;
       if (q8) {
-        p.scale_a = sl + 1;
+        p.amax_a = am_qkv;
         p.scale_b = W.s_qkv;
       }
-      wb_status st = dense_gemm(q8 ? static_cast<const void*>(aq) : a, W.w_qkv, M, 3 * D, D, q8, p, s, PC_ENC_QKV);
+      wb_status st = dense_gemm(q8 ? static_cast<const void*>(aq) : a, W.w_qkv, M, 3 * D, D, q8, EPI_BIAS, qk, 2 * D,
+                                2 * D, nullptr, p, s, PC_ENC_QKV);
       if (st != WB_OK) return st;
     }
     {
@@ -604,67 +619,62 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     }
     if (o8) {
       Prof pr(PC_ENC_QUANT, s, 2);
-      WB_CUDA(launch_amax(o, static_cast<long long>(M) * D, sl + 2, s));
-      WB_CUDA(launch_quantize(o, static_cast<long long>(M) * D, aq, sl + 2, sl + 3, s));
+      WB_CUDA(launch_amax_items(o, static_cast<long long>(M) * D, D, T_TOK, am_out, s));
+      WB_CUDA(launch_quantize_rows(o, static_cast<long long>(M) * D, D, T_TOK, am_out, aq, s));
     }
     {  // out projection + bias + residual -> h
       GemmParams p = base_params();
-      p.out = h;
-      p.ldo = D;
       p.bias = W.b_out;
-      p.resid = src;
       if (o8) {
-        p.scale_a = sl + 3;
+        p.amax_a = am_out;
         p.scale_b = W.s_out;
       }
-      wb_status st = dense_gemm(o8 ? static_cast<const void*>(aq) : o, W.w_out, M, D, D, o8, p, s, PC_ENC_OUT);
+      wb_status st = dense_gemm(o8 ? static_cast<const void*>(aq) : o, W.w_out, M, D, D, o8, EPI_BIAS_RESID, h, D, D,
+                                src, p, s, PC_ENC_OUT);
       if (st != WB_OK) return st;
     }
     // LN2 -> a [-> E4M3]
     {
       Prof pr(PC_ENC_LN, s);
-      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? sl + 4 : nullptr, s));
+      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? am_fc1 : nullptr, T_TOK, s));
     }
     if (f8) {
       Prof pr(PC_ENC_QUANT, s);
-      WB_CUDA(launch_quantize(a, static_cast<long long>(M) * D, aq, sl + 4, sl + 5, s));
+      WB_CUDA(launch_quantize_rows(a, static_cast<long long>(M) * D, D, T_TOK, am_fc1, aq, s));
     }
     {  // FC1 + bias + GELU -> g
       GemmParams p = base_params();
-      p.out = g;
-      p.ldo = F;
       p.bias = W.b_fc1;
-      p.act_gelu = 1;
       if (f8) {
-        p.scale_a = sl + 5;
+        p.amax_a = am_fc1;
         p.scale_b = W.s_fc1;
-        p.amax = sl + 6;
+        p.amax = am_fc2;
       }
-      wb_status st = dense_gemm(f8 ? static_cast<const void*>(aq) : a, W.w_fc1, M, F, D, f8, p, s, PC_ENC_FC1);
+      wb_status st = dense_gemm(f8 ? static_cast<const void*>(aq) : a, W.w_fc1, M, F, D, f8, EPI_BIAS_GELU, g, F, F,
+                                nullptr, p, s, PC_ENC_FC1);
       if (st != WB_OK) return st;
     }
     if (f8) {
       Prof pr(PC_ENC_QUANT, s);
-      WB_CUDA(launch_quantize(g, static_cast<long long>(M) * F, gq, sl + 6, sl + 7, s));
+      WB_CUDA(launch_quantize_rows(g, static_cast<long long>(M) * F, F, T_TOK, am_fc2, gq, s));
     }
     {  // FC2 + bias + residual -> h (or straight to out after the last layer without final LN)
       GemmParams p = base_params();
-      p.out = (last && !apply_final_ln) ? outb : h;
-      p.ldo = D;
       p.bias = W.b_fc2;
-      p.resid = h;
       if (f8) {
-        p.scale_a = sl + 7;
+        p.amax_a = am_fc2;
         p.scale_b = W.s_fc2;
       }
-      wb_status st = dense_gemm(f8 ? static_cast<const void*>(gq) : g, W.w_fc2, M, D, F, f8, p, s, PC_ENC_FC2);
+      void* dst = (last && !apply_final_ln) ? static_cast<void*>(outb) : static_cast<void*>(h);
+      wb_status st = dense_gemm(f8 ? static_cast<const void*>(gq) : g, W.w_fc2, M, D, F, f8, EPI_BIAS_RESID, dst, D, D,
+                                h, p, s, PC_ENC_FC2);
       if (st != WB_OK) return st;
     }
   }
   const __nv_bfloat16* final_src = n_layers_run > 0 ? h : x0b;
   if (apply_final_ln) {
     Prof pr(PC_ENC_LN, s);
-    WB_CUDA(launch_layernorm(final_src, nullptr, ln_post->g, ln_post->b, M, D, eps, outb, nullptr, nullptr, s));
+    WB_CUDA(launch_layernorm(final_src, nullptr, ln_post->g, ln_post->b, M, D, eps, outb, nullptr, nullptr, 0, s));
   } else if (n_layers_run == 0) {
     WB_CUDA(cudaMemcpyAsync(outb, x0b, static_cast<size_t>(M) * D * 2, cudaMemcpyDeviceToDevice, s));
   }
@@ -707,16 +717,14 @@ wb_status wb_linear(const void* a, const void* w, int M, int N, int K, int dtype
   if (resid && !aligned16(resid)) return WB_EINVAL;
   if (fp8 && (!scale_a || !scale_w)) return WB_EINVAL;
   GemmParams p = base_params();
-  p.out = out;
-  p.ldo = N;
   p.bias = bias;
   p.act_gelu = gelu ? 1 : 0;
-  p.resid = static_cast<const __nv_bfloat16*>(resid);
   if (fp8) {
     p.scale_a = scale_a;
     p.scale_b = scale_w;
   }
-  return dense_gemm(a, w, M, N, K, fp8, p, static_cast<cudaStream_t>(stream));
+  const int epi = resid ? EPI_BIAS_RESID : gelu ? EPI_BIAS_GELU : EPI_BIAS;
+  return dense_gemm(a, w, M, N, K, fp8, epi, out, N, N, resid, p, static_cast<cudaStream_t>(stream));
 }
 
 wb_status wb_layernorm(const void* x, const void* residual, const float* g, const float* b, int rows, int d,
@@ -726,7 +734,7 @@ wb_status wb_layernorm(const void* x, const void* residual, const float* g, cons
   if (!x || !g || !b || !y || !aligned16(x) || !aligned16(y)) return WB_EINVAL;
   if ((residual && !aligned16(residual)) || (total && (!residual || !aligned16(total)))) return WB_EINVAL;
   WB_CUDA(launch_layernorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(residual), g, b,
-                           rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total), nullptr,
+                           rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total), nullptr, 0,
                            static_cast<cudaStream_t>(stream)));
   return WB_OK;
 }

@@ -8,10 +8,13 @@
 //   * the conv stem as an implicit GEMM (one pass per kernel tap),
 //   * the windowed real DFT and the mel filterbank (split-bf16 passes).
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA loads into a ring of smem
+// Roles (576 threads): warp 0 lane 0 issues TMA loads into a ring of smem
 // stages; warp 1 lane 0 issues tcgen05.mma into one of two TMEM accumulators;
-// warps 2-5 (128 threads, one accumulator row each) run the epilogue of tile
-// i while the MMA warp already accumulates tile i+1.  All waits are bounded.
+// warps 2-17 run the epilogue of tile i while the MMA warp already
+// accumulates tile i+1.  Epilogue warp w owns TMEM lane quarter w%4 (32 rows)
+// and one quarter of the tile's columns; it stages its 32x32 output boxes in
+// shared memory and writes them with TMA bulk stores (residual boxes arrive
+// the same way).  All waits are bounded.
 //
 // K schedule: a list of passes; pass p reads A through tensor map amap[p]
 // (4-D: k, row, part, batch) at row offset a_row_off and part a_part, and B
@@ -29,8 +32,11 @@ struct GemmSmem {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int TOTAL = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int EPI_BOX_BYTES = 32 * 64;   // one 32 x 32 bf16 box per epilogue warp (64-byte swizzle)
+  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_EPI + GEMM_EPI_WARPS * EPI_BOX_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int TOTAL = 1024 + OFF_BAR + BAR_BYTES;
 };
 
 __device__ __forceinline__ float sinusoid(int t, int n, int d) {
@@ -41,28 +47,37 @@ __device__ __forceinline__ float sinusoid(int t, int n, int d) {
   return n < half ? sinf(ang) : cosf(ang);
 }
 
+// Byte offset of 16-byte chunk j (columns 8j..8j+7) of row r in a 32 x 64-byte box stored with
+// the 64-byte swizzle (chunk index XOR address bits 7-8), as TMA reads and writes it.
+__device__ __forceinline__ uint32_t box_off(int r, int j) {
+  return static_cast<uint32_t>(r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+}
+
 template <int BN, bool FP8, int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap amap0, const __grid_constant__ CUtensorMap amap1,
                 const __grid_constant__ CUtensorMap amap2, const __grid_constant__ CUtensorMap amap3,
-                const __grid_constant__ CUtensorMap bmap, const __grid_constant__ GemmParams p) {
+                const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap omap,
+                const __grid_constant__ CUtensorMap rmap, const __grid_constant__ GemmParams p) {
   using S = GemmSmem<BN>;
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC = make_idesc(GEMM_BM, BN, FP8 ? 0u : 1u);
   constexpr int KSTEPS = 4;  // 128-byte rows: 4 x K16 (bf16) or 4 x K32 (E4M3)
   constexpr int BK = FP8 ? 128 : 64;
   constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr bool STD = EPI == EPI_BIAS || EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_RESID || EPI == EPI_CONV2;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base_u32 - smem_u32(smem_raw));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
-  uint64_t* full = bars;                 // [STAGES]
-  uint64_t* empty = bars + STAGES;       // [STAGES]
-  uint64_t* tfull = bars + 2 * STAGES;   // [2]
-  uint64_t* tempty = tfull + 2;          // [2]
-  uint64_t* mma_done = tempty + 2;       // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
+  uint64_t* full = bars;                       // [STAGES]
+  uint64_t* empty = bars + STAGES;             // [STAGES]
+  uint64_t* tfull = bars + 2 * STAGES;         // [2]
+  uint64_t* tempty = tfull + 2;                // [2]
+  uint64_t* mma_done = tempty + 2;             // [1]
+  uint64_t* rbar = mma_done + 1;               // [GEMM_EPI_WARPS] residual box arrivals
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + GEMM_EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
@@ -75,9 +90,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], GEMM_EPI_WARPS);
     }
     mbar_init(mma_done, 1);
+    for (int w = 0; w < GEMM_EPI_WARPS; ++w) mbar_init(&rbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -166,92 +182,151 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------- epilogue ------------------------------
-    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    const int row_in_tile = quarter * 32 + lane;
+    constexpr int COLS = BN / 4;                 // columns per epilogue warp
+    constexpr int CHUNKS = COLS / 32;
+    const int ew = warp - 2;                     // 0 .. GEMM_EPI_WARPS-1
+    const int quarter = warp & 3;                // TMEM lane quarter this warp may access
+    const int cg = ew >> 2;                      // column group
+    uint8_t* box = smem + S::OFF_EPI + ew * S::EPI_BOX_BYTES;
+    uint32_t rphase = 0;
+    bool ok = true;
     int local = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
+    float alpha_w = 1.0f, alpha_a = 1.0f;
+    if (FP8) {
+      if (p.scale_a) alpha_a = *p.scale_a;
+      if (p.scale_b) alpha_w = *p.scale_b;
+    }
+
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, p.err, abort_flag, 4)) break;
-      tc_fence_after();
       const int b = tile / tiles_per_item;
       const int r = tile % tiles_per_item;
       const int mt = r / n_tiles, nt = r % n_tiles;
-      const int m = mt * GEMM_BM + row_in_tile;
+      const int m0 = mt * GEMM_BM + quarter * 32;      // first row of this warp's slab
+      const int m = m0 + lane;
       const bool row_ok = m < p.M;
+      const int ncol0 = nt * BN + cg * COLS;
+      // residual box of the first chunk: fetch while the accumulator is still being computed
+      if (EPI == EPI_BIAS_RESID && lane == 0 && ncol0 < p.N) {
+        bulk_wait_read0();
+        mbar_arrive_expect_tx(&rbar[ew], S::EPI_BOX_BYTES);
+        tma_load_3d(box, &rmap, &rbar[ew], ncol0, p.out_row_off + m0, b);
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, p.err, abort_flag, 4)) { ok = false; break; }
+      tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 
-      if constexpr (EPI == EPI_STD) {
-        float alpha = 1.0f;
-        if (p.scale_a) alpha *= *p.scale_a;
-        if (p.scale_b) alpha *= *p.scale_b;
-        float local_amax = 0.0f;
-        const long long orow = static_cast<long long>(b) * p.out_batch_rows + p.out_row_off + m;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int n0 = nt * BN + c * 32;
+      if constexpr (STD) {
+        // flattened row -> batch item (chunk) for the per-item E4M3 scales
+        const int item = p.rows_per_item > 0 ? (b * p.M + (row_ok ? m : p.M - 1)) / p.rows_per_item : 0;
+        float alpha = alpha_w * alpha_a;
+        if (FP8 && p.amax_a) {
+          const float am = __ldg(p.amax_a + item);
+          alpha = alpha_w * (am > 0.0f ? am / 448.0f : 1.0f);
+        }
+        float tile_amax = 0.0f;
+        float v[CHUNKS][32];
+#pragma unroll
+        for (int c = 0; c < CHUNKS; ++c) tmem_ld32(t_row + cg * COLS + c * 32, v[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is free for tile i+2
+#pragma unroll
+        for (int c = 0; c < CHUNKS; ++c) {
+          const int n0 = ncol0 + c * 32;
           if (n0 >= p.N) break;
-          float v[32];
-          tmem_ld32(t_row + c * 32, v);
-          tmem_ld_wait();
-          if (!row_ok) continue;
+          // bias (+ E4M3 scale) and activation
+          const float4* bp = reinterpret_cast<const float4*>(p.bias + n0);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x = v[i] * alpha;
-            if (p.bias) x += __ldg(p.bias + n0 + i);
-            if (p.act_gelu) x = gelu_erf(x);
-            if (p.add_pe) x += sinusoid(m, n0 + i, p.N);
-            v[i] = x;
-          }
-          if (p.vt && n0 >= p.vt_col0) {
-            // V goes out transposed: row (b*H + h)*64 + e, column t
-            const int col = n0 - p.vt_col0;
-            const int gb = (b * p.M + m) / p.vt_T, t = (b * p.M + m) % p.vt_T;
-            const int h = col >> 6, e0 = col & 63;
-            const int H = (p.N - p.vt_col0) >> 6;
-            __nv_bfloat16* dst = p.vt + (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 bb = p.bias ? __ldg(bp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[static_cast<long long>(i) * p.vt_ld] = __float2bfloat16_rn(v[i]);
-            continue;
-          }
-          if (p.resid) {
-            const uint4* rp = reinterpret_cast<const uint4*>(p.resid + orow * p.ldo + n0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 u = rp[j];
-              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&u);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[j * 8 + i] += __bfloat162float(hv[i]);
+            for (int k = 0; k < 4; ++k) {
+              float x = FP8 ? fmaf(v[c][4 * i4 + k], alpha, bv[k]) : v[c][4 * i4 + k] + bv[k];
+              if (EPI == EPI_BIAS_GELU || EPI == EPI_CONV2) x = gelu_fast(x);
+              if (EPI == EPI_BIAS_RESID && p.act_gelu) x = gelu_fast(x);
+              if (EPI == EPI_CONV2) x += sinusoid(m, n0 + 4 * i4 + k, p.N);
+              v[c][4 * i4 + k] = x;
             }
           }
-          uint4 pk[4];
-          uint32_t* pw32 = reinterpret_cast<uint32_t*>(pk);
+          if (EPI == EPI_BIAS && p.vt && n0 >= p.vt_col0) {
+            // V goes out transposed: row (b*H + h)*64 + e, column t (32 lanes = 32 consecutive t)
+            if (row_ok) {
+              const int col = n0 - p.vt_col0;
+              const int gb = m / p.vt_T, t = m % p.vt_T;
+              const int h = col >> 6, e0 = col & 63;
+              const int H = (p.N - p.vt_col0) >> 6;
+              __nv_bfloat16* dst = p.vt + (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pw32[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-          if (p.amax) {
-            const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(pk);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) local_amax = fmaxf(local_amax, fabsf(__bfloat162float(hv[i])));
+              for (int i = 0; i < 32; ++i) dst[static_cast<long long>(i) * p.vt_ld] = __float2bfloat16_rn(v[c][i]);
+            }
+            continue;
           }
-          uint4* op = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * p.ldo + n0);
+          if (EPI == EPI_BIAS_RESID) {
+            if (!mbar_wait(&rbar[ew], rphase, p.err, abort_flag, 5)) { ok = false; break; }
+            rphase ^= 1u;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) op[j] = pk[j];
+            for (int j = 0; j < 4; ++j) {
+              const uint4 u = *reinterpret_cast<const uint4*>(box + box_off(lane, j));
+              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[c][8 * j + i] += __bfloat162float(hv[i]);
+            }
+          } else {
+            if (lane == 0) bulk_wait_read0();       // previous store has read the box
+            __syncwarp();
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[c][2 * i], v[c][2 * i + 1]);
+          if (p.amax && row_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&pk[i]);
+              tile_amax = fmaxf(tile_amax, fmaxf(fabsf(__bfloat162float(hv.x)), fabsf(__bfloat162float(hv.y))));
+            }
+          }
+          __syncwarp();   // every lane has read the residual box before it is overwritten
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(box + box_off(lane, j)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&omap, box, n0, p.out_row_off + m0, b);
+            bulk_commit();
+            // residual box of the next chunk of this tile goes into the same buffer
+            if (EPI == EPI_BIAS_RESID && c + 1 < CHUNKS && n0 + 32 < p.N) {
+              bulk_wait_read0();
+              mbar_arrive_expect_tx(&rbar[ew], S::EPI_BOX_BYTES);
+              tma_load_3d(box, &rmap, &rbar[ew], n0 + 32, p.out_row_off + m0, b);
+            }
+          }
         }
-        if (p.amax) {
+        if (p.amax) {   // one atomic per warp and tile; per lane where the 32 rows straddle two chunks
+          const int item0 = __shfl_sync(0xffffffffu, item, 0);
+          if (__all_sync(0xffffffffu, item == item0)) {
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) local_amax = fmaxf(local_amax, __shfl_xor_sync(0xffffffffu, local_amax, o));
-          if (lane == 0 && local_amax > 0.0f) atomic_max_nonneg(p.amax, local_amax);
+            for (int o = 16; o > 0; o >>= 1) tile_amax = fmaxf(tile_amax, __shfl_xor_sync(0xffffffffu, tile_amax, o));
+            if (lane == 0 && tile_amax > 0.0f) atomic_max_nonneg(p.amax + item0, tile_amax);
+          } else if (tile_amax > 0.0f) {
+            atomic_max_nonneg(p.amax + item, tile_amax);
+          }
         }
       } else if constexpr (EPI == EPI_POWER) {
-        // columns [0, BN/2) hold the cosine part and [BN/2, BN) the sine part of the same bins
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          float re[32], im[32];
-          tmem_ld32(t_row + c * 32, re);
-          tmem_ld32(t_row + BN / 2 + c * 32, im);
-          tmem_ld_wait();
-          if (!row_ok) continue;
-          const int bin0 = nt * (BN / 2) + c * 32;
+        // cosine part in columns [0, BN/2), sine part of the same bins in [BN/2, BN); warp cg owns 32 bins
+        float re[32], im[32];
+        tmem_ld32(t_row + cg * 32, re);
+        tmem_ld32(t_row + BN / 2 + cg * 32, im);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (row_ok) {
+          const int bin0 = nt * (BN / 2) + cg * 32;
           uint4 hi[4], lo[4];
           uint32_t* h32 = reinterpret_cast<uint32_t*>(hi);
           uint32_t* l32 = reinterpret_cast<uint32_t*>(lo);
@@ -272,15 +347,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             dl[j] = lo[j];
           }
         }
-      } else {  // EPI_MEL
+      } else {  // EPI_MEL: warp cg owns 32 mel bins
+        float v[32];
+        tmem_ld32(t_row + cg * 32, v);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        const int n0 = nt * BN + cg * 32;
         float local_max = 0.0f;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int n0 = nt * BN + c * 32;
-          float v[32];
-          tmem_ld32(t_row + c * 32, v);
-          tmem_ld_wait();
-          if (!row_ok || n0 >= p.n_valid) continue;
+        if (row_ok && n0 < p.n_valid) {
           float* dst = p.mel_out + (static_cast<long long>(b) * p.n_valid + n0) * p.M + m;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -295,9 +371,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int o = 16; o > 0; o >>= 1) local_max = fmaxf(local_max, __shfl_xor_sync(0xffffffffu, local_max, o));
         if (lane == 0 && local_max > 0.0f) atomic_max_nonneg(p.mel_max + b, local_max);
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
     }
+
+    if (lane == 0) bulk_wait0();   // stores complete before the CTA (and its smem) goes away
+    if (!ok && EPI == EPI_BIAS_RESID && lane == 0) mbar_drain(&rbar[ew], rphase);
   }
 
   tc_fence_before();

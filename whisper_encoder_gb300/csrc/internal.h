@@ -31,7 +31,11 @@ cudaError_t launch_stem_transpose(const float* logmel, int batch, int n_mels, __
 cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16* packed, cudaStream_t s);
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
                              int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             cudaStream_t s);
+                             int rows_per_item, cudaStream_t s);
+cudaError_t launch_quantize_rows(const __nv_bfloat16* x, long long n, int cols, int rows_per_item,
+                                 const float* amax, uint8_t* q, cudaStream_t s);
+cudaError_t launch_amax_items(const __nv_bfloat16* x, long long n, int cols, int rows_per_item, float* amax,
+                              cudaStream_t s);
 cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaStream_t s);
 cudaError_t launch_quantize(const __nv_bfloat16* x, long long n, uint8_t* q, const float* amax,
                             float* scale_out, cudaStream_t s);
@@ -47,6 +51,8 @@ cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long
 struct GemmLaunch {
   CUtensorMap amap[GEMM_MAX_AMAPS];
   CUtensorMap bmap;
+  CUtensorMap omap;   // output boxes (32 x 32 bf16, 64-byte swizzle), standard epilogues only
+  CUtensorMap rmap;   // residual boxes (EPI_BIAS_RESID)
   GemmParams p;
   int bn;       // 128 or 256
   bool fp8;

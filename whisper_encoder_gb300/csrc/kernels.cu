@@ -171,16 +171,26 @@ struct VecIO<4> {
   using T = uint2;
 };
 
+constexpr int LN_WARPS = 8;
+
+// amax (optional): per-item absmax of the bf16 outputs, item = row / rows_per_item.
 template <int NV, int VEC>
 __global__ void layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
                                  const float* __restrict__ g, const float* __restrict__ bta, int rows, float eps,
                                  __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ total,
-                                 float* __restrict__ amax) {
+                                 float* __restrict__ amax, int rows_per_item) {
   constexpr int D = NV * VEC * 32;
   using V = typename VecIO<VEC>::T;
+  __shared__ float w_max[LN_WARPS];
   const int lane = threadIdx.x & 31;
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (row >= rows) return;
+  if (row >= rows) {
+    if (amax) {
+      if (lane == 0) w_max[threadIdx.x >> 5] = 0.0f;
+      __syncthreads();
+    }
+    return;
+  }
   float v[NV * VEC];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -240,7 +250,23 @@ __global__ void layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv
   if (amax) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0 && mx > 0.0f) atomic_max_nonneg(amax, mx);
+    if (lane == 0) w_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {   // the block's 8 rows span at most two items: merge, then 1-2 atomics
+      const long long row0 = static_cast<long long>(blockIdx.x) * LN_WARPS;
+      int cur = static_cast<int>(row0 / rows_per_item);
+      float m = 0.0f;
+      for (int w = 0; w < LN_WARPS && row0 + w < rows; ++w) {
+        const int it = static_cast<int>((row0 + w) / rows_per_item);
+        if (it != cur) {
+          if (m > 0.0f) atomic_max_nonneg(amax + cur, m);
+          cur = it;
+          m = 0.0f;
+        }
+        m = fmaxf(m, w_max[w]);
+      }
+      if (m > 0.0f) atomic_max_nonneg(amax + cur, m);
+    }
   }
 }
 
@@ -297,6 +323,61 @@ __global__ void quantize_kernel(const __nv_bfloat16* __restrict__ x, long long n
   }
   for (long long i = n16 * 16 + tid; i < n; i += step)
     q[i] = static_cast<uint8_t>(cvt_e4m3x2(__bfloat162float(x[i]) * inv, 0.0f) & 0xFF);
+}
+
+// Activation quantiser with one scale per batch item: rows of `cols` elements, item = row /
+// rows_per_item, code = E4M3_rn_satfinite(x * inv_item), inv_item = 448 / amax[item] (1 if 0).
+__global__ void quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, long long n, int cols, int rows_per_item,
+                                     const float* __restrict__ amax, uint8_t* __restrict__ q) {
+  const long long n16 = n / 16;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = tid; i < n16; i += step) {
+    const int item = static_cast<int>((i * 16) / cols / rows_per_item);
+    const float a = __ldg(amax + item);
+    const float inv = a > 0.0f ? 448.0f / a : 1.0f;
+    const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * i;
+    uint4 u0 = src[0], u1 = src[1];
+    const __nv_bfloat16* h0 = reinterpret_cast<const __nv_bfloat16*>(&u0);
+    const __nv_bfloat16* h1 = reinterpret_cast<const __nv_bfloat16*>(&u1);
+    uint4 o;
+    uint16_t* o16 = reinterpret_cast<uint16_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o16[j] = cvt_e4m3x2(__bfloat162float(h0[2 * j]) * inv, __bfloat162float(h0[2 * j + 1]) * inv);
+      o16[4 + j] = cvt_e4m3x2(__bfloat162float(h1[2 * j]) * inv, __bfloat162float(h1[2 * j + 1]) * inv);
+    }
+    reinterpret_cast<uint4*>(q)[i] = o;
+  }
+}
+
+// Per-item absmax of a [rows, cols] bf16 tensor (item = row / rows_per_item), 8 elements per step.
+__global__ void amax_items_kernel(const __nv_bfloat16* __restrict__ x, long long n, int cols, int rows_per_item,
+                                  float* __restrict__ amax) {
+  const long long n8 = n / 8;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = blockIdx.x * static_cast<long long>(blockDim.x); base < n8; base += step) {
+    const long long i = base + threadIdx.x;
+    float m = 0.0f;
+    int item = -1;
+    if (i < n8) {
+      item = static_cast<int>((i * 8) / cols / rows_per_item);
+      uint4 u = reinterpret_cast<const uint4*>(x)[i];
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(__bfloat162float(h[j])));
+    }
+    const int item0 = __shfl_sync(0xffffffffu, item, 0);
+    if (__all_sync(0xffffffffu, item == item0)) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if ((threadIdx.x & 31) == 0 && item0 >= 0 && m > 0.0f) atomic_max_nonneg(amax + item0, m);
+    } else if (item >= 0 && m > 0.0f) {
+      atomic_max_nonneg(amax + item, m);
+    }
+  }
+  (void)tid;
 }
 
 __global__ void finalize_scale_kernel(float* p) {
@@ -390,19 +471,18 @@ cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16*
 template <int NV, int VEC>
 static cudaError_t ln_launch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
                              int rows, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             cudaStream_t s) {
-  const int warps = 8;
-  layernorm_kernel<NV, VEC><<<(rows + warps - 1) / warps, warps * 32, 0, s>>>(x, res, g, b, rows, eps, y, total,
-                                                                               amax);
+                             int rows_per_item, cudaStream_t s) {
+  layernorm_kernel<NV, VEC><<<(rows + LN_WARPS - 1) / LN_WARPS, LN_WARPS * 32, 0, s>>>(
+      x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
   return cudaGetLastError();
 }
 
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
                              int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             cudaStream_t s) {
+                             int rows_per_item, cudaStream_t s) {
 #define WB_LN_CASE(NV, VEC) \
   case NV * VEC * 32:       \
-    return ln_launch<NV, VEC>(x, res, g, b, rows, eps, y, total, amax, s);
+    return ln_launch<NV, VEC>(x, res, g, b, rows, eps, y, total, amax, rows_per_item, s);
   switch (d) {
     WB_LN_CASE(1, 4)
     WB_LN_CASE(1, 8)
@@ -434,6 +514,19 @@ cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaSt
 cudaError_t launch_quantize(const __nv_bfloat16* x, long long n, uint8_t* q, const float* amax, float* scale_out,
                             cudaStream_t s) {
   quantize_kernel<<<grid_for(n / 16 + 1, EW_THREADS, 152 * 16), EW_THREADS, 0, s>>>(x, n, q, amax, scale_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const __nv_bfloat16* x, long long n, int cols, int rows_per_item,
+                                 const float* amax, uint8_t* q, cudaStream_t s) {
+  quantize_rows_kernel<<<grid_for(n / 16 + 1, EW_THREADS, 152 * 16), EW_THREADS, 0, s>>>(x, n, cols, rows_per_item,
+                                                                                        amax, q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_items(const __nv_bfloat16* x, long long n, int cols, int rows_per_item, float* amax,
+                              cudaStream_t s) {
+  amax_items_kernel<<<grid_for(n / 8 + 1, EW_THREADS, 152 * 8), EW_THREADS, 0, s>>>(x, n, cols, rows_per_item, amax);
   return cudaGetLastError();
 }
 

@@ -30,21 +30,33 @@ cudaError_t gemm_launch_t(const GemmLaunch& g, cudaStream_t s) {
   int grid = sm_count();
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid < 1) return cudaSuccess;
-  kern<<<grid, GEMM_THREADS, smem, s>>>(g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap, g.p);
+  kern<<<grid, GEMM_THREADS, smem, s>>>(g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap, g.omap, g.rmap, g.p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  if (g.epi == EPI_STD) {
-    if (g.bn == 256) return g.fp8 ? gemm_launch_t<256, true, EPI_STD>(g, s) : gemm_launch_t<256, false, EPI_STD>(g, s);
-    if (g.bn == 128) return g.fp8 ? gemm_launch_t<128, true, EPI_STD>(g, s) : gemm_launch_t<128, false, EPI_STD>(g, s);
-  } else if (g.epi == EPI_POWER && g.bn == 256 && !g.fp8) {
-    return gemm_launch_t<256, false, EPI_POWER>(g, s);
-  } else if (g.epi == EPI_MEL && g.bn == 128 && !g.fp8) {
-    return gemm_launch_t<128, false, EPI_MEL>(g, s);
+#define WB_GEMM_STD(BN)                                                                                        \
+  switch (g.epi) {                                                                                             \
+    case EPI_BIAS: return g.fp8 ? gemm_launch_t<BN, true, EPI_BIAS>(g, s) : gemm_launch_t<BN, false, EPI_BIAS>(g, s); \
+    case EPI_BIAS_GELU:                                                                                        \
+      return g.fp8 ? gemm_launch_t<BN, true, EPI_BIAS_GELU>(g, s) : gemm_launch_t<BN, false, EPI_BIAS_GELU>(g, s); \
+    case EPI_BIAS_RESID:                                                                                       \
+      return g.fp8 ? gemm_launch_t<BN, true, EPI_BIAS_RESID>(g, s) : gemm_launch_t<BN, false, EPI_BIAS_RESID>(g, s); \
+    case EPI_CONV2:                                                                                            \
+      if (!g.fp8) return gemm_launch_t<BN, false, EPI_CONV2>(g, s);                                           \
+      break;                                                                                                   \
+    default: break;                                                                                            \
   }
+  if (g.bn == 256) {
+    WB_GEMM_STD(256)
+    if (g.epi == EPI_POWER && !g.fp8) return gemm_launch_t<256, false, EPI_POWER>(g, s);
+  } else if (g.bn == 128) {
+    WB_GEMM_STD(128)
+    if (g.epi == EPI_MEL && !g.fp8) return gemm_launch_t<128, false, EPI_MEL>(g, s);
+  }
+#undef WB_GEMM_STD
   return cudaErrorInvalidValue;
 }
 

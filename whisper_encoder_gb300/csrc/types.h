@@ -10,11 +10,20 @@ namespace wb {
 enum : uint32_t { ERR_TIMEOUT = 1u, ERR_BOUNDS = 2u };
 
 constexpr int GEMM_BM = 128;
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_EPI_WARPS = 16;                      // 4 per TMEM lane quarter
+constexpr int GEMM_THREADS = 64 + 32 * GEMM_EPI_WARPS;   // producer + MMA + epilogue warps
 constexpr int GEMM_MAX_PASSES = 24;
 constexpr int GEMM_MAX_AMAPS = 4;
 
-enum EpiKind : int { EPI_STD = 0, EPI_POWER = 1, EPI_MEL = 2 };
+// Epilogue kinds (compile-time): what happens to each fp32 accumulator after the mainloop.
+enum EpiKind : int {
+  EPI_BIAS = 0,        // y = alpha*acc + bias                     (QKV with the V^T side output, plain linear)
+  EPI_BIAS_GELU = 1,   // y = GELU(alpha*acc + bias)               (FC1, conv1)
+  EPI_BIAS_RESID = 2,  // y = [GELU](alpha*acc + bias) + resid     (out-proj, FC2)
+  EPI_CONV2 = 3,       // y = GELU(acc + bias) + sinusoid(row, col) (conv2)
+  EPI_POWER = 4,       // DFT: |X|^2 split into bf16 hi/lo parts
+  EPI_MEL = 5          // mel: log10(max(acc, 1e-10)) written transposed, per-item max
+};
 
 struct GemmPass {
   int8_t amap, a_part, a_row_off, b_part;
@@ -28,18 +37,16 @@ struct GemmParams {
   int batch;         // batch items (A's 4th tensor-map coordinate)
   int n_pass;
   GemmPass pass[GEMM_MAX_PASSES];
-  // ---- standard epilogue: y = act(alpha * acc + bias) (+ pe) (+ resid) ----
-  void* out;                 // bf16 output
-  long long ldo;             // elements between output rows
-  long long out_batch_rows;  // output rows between batch items
-  int out_row_off;           // extra row offset inside a batch item
+  // ---- standard epilogues: the output (and residual) tiles move through TMA maps ----
+  int out_row_off;           // row offset of row 0 of an item inside the output map
   const float* bias;         // [N] or null
   const float* scale_a;      // device scalars multiplied into alpha (E4M3 operand scales) or null
   const float* scale_b;
-  int act_gelu;              // 1: exact-erf GELU after the bias
-  int add_pe;                // 1: add the sinusoidal position table (row = position, col = channel)
-  const __nv_bfloat16* resid;  // residual added last, same indexing as out, or null
-  float* amax;               // if set: atomic max of |y| (feeds a per-tensor E4M3 scale)
+  const float* amax_a;       // if set: per-item absmax of the E4M3 A operand; row m of item i is
+                             // scaled by (amax_a[i] > 0 ? amax_a[i] / 448 : 1) instead of *scale_a
+  int rows_per_item;         // rows of one batch item (chunk) in the flattened row index
+  int act_gelu;              // EPI_BIAS_RESID only: GELU before the residual add
+  float* amax;               // if set: per-item atomic max of |y| (feeds the next E4M3 operand's scale)
   // QKV: columns >= vt_col0 are written transposed to vt[(b*H + h)*64 + e][t]
   __nv_bfloat16* vt;
   int vt_col0, vt_T, vt_ld;  // tokens per batch item, elements between vt rows
