@@ -128,6 +128,27 @@ size_t wb_logmel_workspace_bytes(int n_chunks, int n_mels);
 wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride, int n_chunks, int n_mels,
                     float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* --- log-mel without a workspace -----------------------------------------------
+ * The source pages have no counterpart to this entry point.  It is for callers
+ * that cannot allocate device memory: a real-time audio thread must not block
+ * in cudaMalloc (which can synchronize the device), and plugin hosts or
+ * serving runtimes that own every device buffer forbid their plugins to
+ * allocate.  It computes exactly what wb_logmel computes, but takes its
+ * scratch from one fixed array built into the library (about 13 MiB, present
+ * on every device that loads the library until the process exits) instead of
+ * a caller workspace.  It calls no allocating routine.
+ *  - n_chunks above WB_LOGMEL_STATIC_MAX_CHUNKS returns WB_EINVAL before
+ *    anything is launched; other arguments as for wb_logmel.
+ *  - The first call on a device, made with that device current, looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls share the one array per device and it keeps the previous
+ *    call's contents (the call clears what must start at zero itself).  Calls
+ *    whose GPU work overlaps, e.g. on two streams without ordering, race on
+ *    it: issue them on one stream or order them. */
+#define WB_LOGMEL_STATIC_MAX_CHUNKS 2
+wb_status wb_logmel_static(const float* audio, int64_t n_samples, int64_t chunk_stride, int n_chunks, int n_mels,
+                           float* out, void* stream);
+
 /* --- conv stem ---------------------------------------------------------------
  * x0[b] = GELU(conv2(GELU(conv1(logmel[b])))) + sinusoidal positions, with
  * conv1 = Conv1d(n_mels -> d, k3, stride 1, pad 1) and conv2 = Conv1d(d -> d,

@@ -7,4 +7,4 @@ from ._lib import WB_BF16, WB_E4M3, WbError, load  # noqa: F401
 from .api import (  # noqa: F401
     PRESET_BF16, PRESET_MIXED_FP8, EncoderWeights, LayerWeights, Pipeline, StemWeights, attention,
     check_device_error, conv_stem, dequantize_fp8, encoder_forward, encoder_workspace_bytes, layernorm, linear,
-    logmel, logmel_workspace_bytes, pack_conv_weight, profile_begin, profile_end, quantize_fp8, upload_weights)
+    logmel, logmel_static, logmel_workspace_bytes, pack_conv_weight, profile_begin, profile_end, quantize_fp8, upload_weights)

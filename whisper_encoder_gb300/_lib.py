@@ -15,6 +15,7 @@ LIB_PATH = _build.LIB
 
 WB_OK, WB_EINVAL, WB_ECUDA, WB_EUNSUPPORTED, WB_ETIMEOUT, WB_EWORKSPACE = 0, -1, -2, -3, -4, -5
 WB_BF16, WB_E4M3 = 0, 1
+WB_LOGMEL_STATIC_MAX_CHUNKS = 2   # include/wb.h
 
 c_int, c_i64, c_size, c_void, c_float = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 P = ctypes.POINTER
@@ -49,6 +50,7 @@ SIGNATURES = {
     "wb_check_device_error": (c_int, [c_void, P(ctypes.c_uint32)]),
     "wb_logmel_workspace_bytes": (c_size, [c_int, c_int]),
     "wb_logmel": (c_int, [c_void, c_i64, c_i64, c_int, c_int, c_void, c_void, c_size, c_void]),
+    "wb_logmel_static": (c_int, [c_void, c_i64, c_i64, c_int, c_int, c_void, c_void]),
     "wb_conv_stem_workspace_bytes": (c_size, [P(wb_dims), c_int]),
     "wb_conv_stem": (c_int, [c_void, c_int, P(wb_dims), P(wb_stem_weights), c_void, c_void, c_size, c_void]),
     "wb_pack_conv_weight": (c_int, [c_void, c_int, c_int, c_void, c_void]),

@@ -66,6 +66,20 @@ def logmel(audio: torch.Tensor, n_chunks: int, n_mels: int, chunk_stride: int = 
     return out
 
 
+def logmel_static(audio: torch.Tensor, n_chunks: int, n_mels: int, chunk_stride: int = CHUNK_SAMPLES,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """wb_logmel without a workspace: scratch comes from the library's fixed device array.
+
+    For callers that must not allocate device memory; at most
+    WB_LOGMEL_STATIC_MAX_CHUNKS chunks per call, and calls must not overlap on the GPU.
+    (``out`` is allocated here only when the caller passes none.)"""
+    _need(audio, torch.float32, "audio")
+    if out is None:
+        out = torch.empty((n_chunks, n_mels, N_FRAMES), dtype=torch.float32, device=audio.device)
+    call("wb_logmel_static", _p(audio), audio.numel(), chunk_stride, n_chunks, n_mels, _p(out), _stream(stream))
+    return out
+
+
 # ------------------------------- conv stem -----------------------------------
 def pack_conv_weight(w: torch.Tensor, stream=None) -> torch.Tensor:
     """float32 [c_out, c_in, 3] (device) -> bf16 tap-major [3, c_out, c_in]."""
