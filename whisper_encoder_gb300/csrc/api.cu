@@ -50,7 +50,7 @@ bool encoder_fn() {
 
 // rank-dimensional tiled map; strides in bytes for dims 1..rank-1; 128-byte swizzle.
 bool make_map(CUtensorMap* m, bool u8, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
-              const uint32_t* box, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+              const uint32_t* box, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, bool f16 = false) {
   if (!encoder_fn()) return false;
   cuuint64_t gd[5];
   cuuint64_t gs[4];
@@ -61,7 +61,8 @@ bool make_map(CUtensorMap* m, bool u8, int rank, const void* base, const uint64_
     es[i] = 1;
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
-  CUresult r = g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  CUresult r = g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -272,7 +273,7 @@ StemLayout stem_layout(const wb_dims* d, int batch) {
 }
 
 // Attention over q/k row views (row stride ld_qk elements) and V^T.
-wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long long ld_qk, const __nv_bfloat16* vt,
+wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long long ld_qk, const __half* vt,
                         int batch, int T, int H, __nv_bfloat16* out, cudaStream_t s) {
   const uint64_t d = static_cast<uint64_t>(H) * 64;
   CUtensorMap qm, km, vm;
@@ -284,7 +285,7 @@ wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long lon
   const uint64_t vdims[3] = {static_cast<uint64_t>(T), 64, static_cast<uint64_t>(batch) * H};
   const uint64_t vstr[2] = {static_cast<uint64_t>(T_PAD) * 2, static_cast<uint64_t>(T_PAD) * 2 * 64};
   const uint32_t vbox[3] = {64, 64, 1};
-  if (!make_map(&vm, false, 3, vt, vdims, vstr, vbox)) return WB_ECUDA;
+  if (!make_map(&vm, false, 3, vt, vdims, vstr, vbox, CU_TENSOR_MAP_SWIZZLE_128B, true)) return WB_ECUDA;
   AttnParams p;
   p.T = T;
   p.H = H;
@@ -562,7 +563,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
   auto* h = reinterpret_cast<__nv_bfloat16*>(ws + EL.h);
   auto* a = reinterpret_cast<__nv_bfloat16*>(ws + EL.a);
   auto* qk = reinterpret_cast<__nv_bfloat16*>(ws + EL.qk);
-  auto* vt = reinterpret_cast<__nv_bfloat16*>(ws + EL.vt);
+  auto* vt = reinterpret_cast<__half*>(ws + EL.vt);
   auto* o = reinterpret_cast<__nv_bfloat16*>(ws + EL.o);
   auto* g = reinterpret_cast<__nv_bfloat16*>(ws + EL.g);
   auto* aq = EL.aq || pr.qkv_a == WB_E4M3 || pr.out_a == WB_E4M3 || pr.ffn_a == WB_E4M3
@@ -752,7 +753,7 @@ wb_status wb_attention(const void* q, const void* k, const void* v, int batch, i
   if (!workspace || !aligned16(workspace) || workspace_bytes < wb_attention_workspace_bytes(batch, T, n_heads))
     return WB_EWORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto* vt = static_cast<__nv_bfloat16*>(workspace);
+  auto* vt = static_cast<__half*>(workspace);
   const long long d = 64LL * n_heads;
   WB_CUDA(launch_transpose_v(static_cast<const __nv_bfloat16*>(v), d, batch, T, n_heads, vt, s));
   return run_attention(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), d, vt, batch, T,

@@ -2,29 +2,34 @@
 //
 // The whisper-blaze showcase site, "The Solution" (flash_attn_hopper.cu card)
 // and "Impact" ("Attention without the quadratic write"): online softmax over
-// key tiles, scores never written to HBM.  Here rebuilt on tcgen05:
-//   S_j = Q K_j^T      -> TMEM (two 128-column buffers, fp32)
-//   P_j = exp(S_j - m) -> bf16 in shared memory (128-byte swizzled, K-major)
-//   O_j = P_j V_j      -> TMEM (two 64-column buffers), folded into registers
-//                         with the running rescale factor.
-// One CTA owns 128 queries of one (batch, head).  Warp 0 lane 0 loads Q once
-// and a ring of K / V^T tiles with TMA; warp 1 lane 0 issues the MMAs; warps
-// 2-5 own one query row per thread (no cross-thread reductions).  Keys past
-// the sequence end are masked to -inf; rows past it are not stored.
+// key tiles, scores never written to HBM.  Rebuilt on tcgen05:
+//   S_t = Q_t K_j^T        -> TMEM, fp32, one 128-column buffer per query tile
+//   P_t = 2^(S_t c - m_t)  -> f16 in shared memory (packed ex2: two exponentials per MUFU op)
+//   O_t += P_t [V_j | 1]   -> TMEM, fp32, 80 columns: 64 of output and 16 copies of the
+//                             row sum (a block of ones appended to V^T in shared memory)
+// A CTA owns two 128-query tiles of one (batch, head).  Warp 0 lane 0 loads
+// both Q tiles once and a ring of K / V^T tiles with TMA; warp 1 lane 0 issues
+// the MMAs, alternating between the tiles so that one tile's matrix products
+// run while the other tile's softmax runs; warps 2-5 and 6-9 own one query
+// row per thread of tile 0 and tile 1.  The running max m_t is only moved
+// (and O rescaled in TMEM) when a new row maximum exceeds it by more than a
+// factor 2^8, which keeps every P entry below 256.  Keys past the sequence
+// end are masked to -inf; rows past it are not stored.
 #pragma once
 #include "ptx.cuh"
 #include "types.h"
 
 namespace wb {
 
-// q / k maps: 3-D (d, T, batch) views of the query and key rows, box (64, 128, 1)
-// vt map: 3-D (T, 64, batch*H) over V^T [batch*H][64][Tp], box (64, 64, 1)
+// q / k maps: 3-D (d, T, batch) views of the query and key rows (bf16), box (64, 128, 1)
+// vt map: 3-D (T, 64, batch*H) over V^T [batch*H][64][Tp] (f16), box (64, 64, 1)
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap vt_map, const __grid_constant__ AttnParams p) {
   using S = AttnSmem;
-  constexpr uint32_t IDESC_S = make_idesc(128, ATT_BKV, 1u);
-  constexpr uint32_t IDESC_O = make_idesc(128, ATT_HD, 1u);
+  constexpr uint32_t IDESC_S = make_idesc(128, ATT_BKV, 1u);    // bf16 x bf16
+  constexpr uint32_t IDESC_O = make_idesc(128, ATT_NPV, 0u);    // f16 x f16
+  constexpr float RESCALE_LOG2 = 8.0f;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -33,21 +38,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;                  // [STAGES]
   uint64_t* kv_empty = kv_full + ATT_STAGES;     // [STAGES]
-  uint64_t* s_full = kv_empty + ATT_STAGES;      // [2]
-  uint64_t* p_full = s_full + 2;                 // [2]
-  uint64_t* o_full = p_full + 2;                 // [2]
-  uint64_t* o_empty = o_full + 2;                // [2]
-  uint64_t* mma_done = o_empty + 2;
+  uint64_t* s_full = kv_empty + ATT_STAGES;      // [TILES]
+  uint64_t* p_full = s_full + ATT_TILES;         // [TILES]
+  uint64_t* o_done = p_full + ATT_TILES;         // [TILES]
+  uint64_t* mma_done = o_done + ATT_TILES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int n_qt = (p.T + ATT_BQ - 1) / ATT_BQ;
-  const int qt = blockIdx.x % n_qt;
-  const int bh = blockIdx.x / n_qt;
+  const int n_qp = (p.T + ATT_TILES * ATT_BQ - 1) / (ATT_TILES * ATT_BQ);
+  const int qp = blockIdx.x % n_qp;
+  const int bh = blockIdx.x / n_qp;
   const int b = bh / p.H, h = bh % p.H;
-  const int q0 = qt * ATT_BQ;
+  const int q0 = qp * ATT_TILES * ATT_BQ;
   const int nkv = (p.T + ATT_BKV - 1) / ATT_BKV;
 
   if (threadIdx.x == 0) {
@@ -56,42 +60,53 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 128);
+    for (int t = 0; t < ATT_TILES; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (warp >= 2) {
+    // rows 64..79 of every V^T half tile hold f16 ones: their PV columns carry the row sums
+    constexpr int ONES_CHUNKS = (ATT_NPV - ATT_HD) * 128 / 16;     // 16-byte chunks per half tile
+    const int n16 = ATT_STAGES * 2 * ONES_CHUNKS;
+    for (int i = threadIdx.x - 64; i < n16; i += ATT_THREADS - 64) {
+      const int half = i / ONES_CHUNKS, within = i % ONES_CHUNKS;
+      uint8_t* dst = smem + S::OFF_V + half * S::VH_BYTES + ATT_HD * 128 + within * 16;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+    }
+    fence_proxy_async_smem();
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S buffers at 0 and 128, O tiles at 256 and 320.
+  // TMEM columns: S_t at 128 t, O_t at 256 + 128 t (80 columns each).
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&k_map);
       tma_prefetch_desc(&vt_map);
-      mbar_arrive_expect_tx(q_full, S::Q_BYTES);
-      tma_load_3d(smem + S::OFF_Q, &q_map, q_full, h * ATT_HD, q0, b);
+      mbar_arrive_expect_tx(q_full, ATT_TILES * S::Q_BYTES);
+      for (int t = 0; t < ATT_TILES; ++t)
+        tma_load_3d(smem + S::OFF_Q + t * S::Q_BYTES, &q_map, q_full, h * ATT_HD, q0 + t * ATT_BQ, b);
       uint32_t issued = 0, last_par = 0;
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
         const int st = j % ATT_STAGES;
         const uint32_t ph = (j / ATT_STAGES) & 1;
         if (!mbar_wait(&kv_empty[st], ph ^ 1u, p.err, abort_flag, 11)) { ok = false; break; }
-        mbar_arrive_expect_tx(&kv_full[st], S::K_BYTES + S::V_BYTES);
+        mbar_arrive_expect_tx(&kv_full[st], S::K_BYTES + 2 * ATT_HD * 128);
         const int kv0 = j * ATT_BKV;
         tma_load_3d(smem + S::OFF_K + st * S::K_BYTES, &k_map, &kv_full[st], h * ATT_HD, kv0, b);
         uint8_t* vdst = smem + S::OFF_V + st * S::V_BYTES;
         tma_load_3d(vdst, &vt_map, &kv_full[st], kv0, 0, bh);
-        tma_load_3d(vdst + ATT_HD * 128, &vt_map, &kv_full[st], kv0 + 64, 0, bh);
+        tma_load_3d(vdst + S::VH_BYTES, &vt_map, &kv_full[st], kv0 + 64, 0, bh);
         issued |= 1u << st;
         last_par = (last_par & ~(1u << st)) | (ph << st);
       }
@@ -103,129 +118,153 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t sq = smem_u32(smem + S::OFF_Q);
-      bool ok = mbar_wait(q_full, 0, p.err, abort_flag, 12);
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % ATT_STAGES;
-        if (!mbar_wait(&kv_full[st], (j / ATT_STAGES) & 1, p.err, abort_flag, 13)) return false;
-        tc_fence_after();
-        const uint32_t sk = smem_u32(smem + S::OFF_K + st * S::K_BYTES);
-        const uint32_t d_tm = tmem + (j & 1) * ATT_BKV;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mma_bf16(d_tm, sw128_desc(sq + k * 32), sw128_desc(sk + k * 32), IDESC_S, k != 0);
-        mma_commit(&s_full[j & 1]);
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      if (ok && nkv > 1) ok = issue_qk(1);
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j % ATT_STAGES;
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, p.err, abort_flag, 14)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&o_empty[j & 1], ((j - 2) >> 1) & 1, p.err, abort_flag, 15)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t sp = smem_u32(smem + S::OFF_P + (j & 1) * S::P_BYTES);
-        const uint32_t sv = smem_u32(smem + S::OFF_V + st * S::V_BYTES);
-        const uint32_t o_tm = tmem + 256 + (j & 1) * ATT_HD;
+      auto pv = [&](int t, int jj) {
+        const uint32_t sp = smem_u32(smem + S::OFF_P + t * S::P_BYTES);
+        const uint32_t sv = smem_u32(smem + S::OFF_V + (jj % ATT_STAGES) * S::V_BYTES);
+        const uint32_t o_tm = tmem + 256 + t * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t half = (k >> 2) * (ATT_BQ * 128), off = (k & 3) * 32;
-          const uint32_t vhalf = (k >> 2) * (ATT_HD * 128);
-          mma_bf16(o_tm, sw128_desc(sp + half + off), sw128_desc(sv + vhalf + off), IDESC_O, k != 0);
+          const uint32_t off = (k & 3) * 32;
+          mma_bf16(o_tm, sw128_desc(sp + (k >> 2) * (ATT_BQ * 128) + off),
+                   sw128_desc(sv + (k >> 2) * S::VH_BYTES + off), IDESC_O, (jj | k) != 0);
         }
-        mma_commit(&o_full[j & 1]);
-        mma_commit(&kv_empty[st]);
-        if (j + 2 < nkv) ok = issue_qk(j + 2);
+        mma_commit(&o_done[t]);
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag, 12);
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int st = j % ATT_STAGES;
+        if (!mbar_wait(&kv_full[st], (j / ATT_STAGES) & 1, p.err, abort_flag, 13)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sk = smem_u32(smem + S::OFF_K + st * S::K_BYTES);
+        for (int t = 0; t < ATT_TILES && ok; ++t) {
+          if (j > 0) {
+            if (!mbar_wait(&p_full[t], (j - 1) & 1, p.err, abort_flag, 14)) { ok = false; break; }
+            tc_fence_after();
+            pv(t, j - 1);
+          }
+          const uint32_t sq = smem_u32(smem + S::OFF_Q + t * S::Q_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + t * 128, sw128_desc(sq + k * 32), sw128_desc(sk + k * 32), IDESC_S, k != 0);
+          mma_commit(&s_full[t]);
+        }
+        if (ok && j > 0) mma_commit(&kv_empty[(j - 1) % ATT_STAGES]);
+      }
+      for (int t = 0; t < ATT_TILES && ok; ++t) {
+        if (!mbar_wait(&p_full[t], (nkv - 1) & 1, p.err, abort_flag, 15)) { ok = false; break; }
+        tc_fence_after();
+        pv(t, nkv - 1);
       }
       mma_commit(mma_done);
       mbar_drain(mma_done, 0);
     }
   } else {
     // --------------------------- softmax / output --------------------------
+    const int t = (warp - 2) >> 2;                 // query tile of this warpgroup
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;             // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float o_acc[ATT_HD];
-#pragma unroll
-    for (int e = 0; e < ATT_HD; ++e) o_acc[e] = 0.0f;
-    float m_run = -INFINITY, l_run = 0.0f;
-    float alpha_q[2] = {1.0f, 1.0f};
+    const uint32_t s_tm = tmem + lane_off + t * 128;
+    const uint32_t o_tm = tmem + lane_off + 256 + t * 128;
+    uint8_t* pbuf = smem + S::OFF_P + t * S::P_BYTES;
+    const float c = p.scale_log2;
+    float m_use = -INFINITY;
     bool ok = true;
 
-    auto consume_o = [&](int j) -> bool {
-      if (!mbar_wait(&o_full[j & 1], (j >> 1) & 1, p.err, abort_flag, 16)) return false;
-      tc_fence_after();
-      const float a = alpha_q[j & 1];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tmem + lane_off + 256 + (j & 1) * ATT_HD + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o_acc[c * 32 + i] = o_acc[c * 32 + i] * a + v[i];
-      }
-      tc_fence_before();
-      mbar_arrive(&o_empty[j & 1]);
-      return true;
-    };
-
     for (int j = 0; j < nkv && ok; ++j) {
-      if (j >= 2 && !(ok = consume_o(j - 2))) break;
-      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, p.err, abort_flag, 17)) { ok = false; break; }
+      if (!mbar_wait(&s_full[t], j & 1, p.err, abort_flag, 16)) { ok = false; break; }
       tc_fence_after();
       float s[ATT_BKV];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int q = 0; q < 4; ++q) {
         float v[32];
-        tmem_ld32(tmem + lane_off + (j & 1) * ATT_BKV + c * 32, v);
+        tmem_ld32(s_tm + q * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+        for (int i = 0; i < 32; ++i) s[q * 32 + i] = v[i];
       }
       tmem_ld_wait();
       const int valid = min(ATT_BKV, p.T - j * ATT_BKV);
       float mx = -INFINITY;
 #pragma unroll
       for (int i = 0; i < ATT_BKV; ++i) {
-        s[i] = (i < valid) ? s[i] * p.scale_log2 : -INFINITY;
+        s[i] = (i < valid) ? s[i] : -INFINITY;
         mx = fmaxf(mx, s[i]);
       }
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = ex2_approx(m_run - m_new);
-      alpha_q[j & 1] = alpha;
-      m_run = m_new;
-      float sum = 0.0f;
-      uint8_t* pbuf = smem + S::OFF_P + (j & 1) * S::P_BYTES;
+      const float m_cand = mx * c;
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (j == 0) {
+        m_use = m_cand;
+      } else if (m_cand > m_use + RESCALE_LOG2) {
+        alpha = ex2_approx(m_use - m_cand);
+        m_use = m_cand;
+        rescale = true;
+      }
+      if (j > 0) {
+        // PV of the previous step is complete: P may be overwritten and O is stable until PV(j) is issued
+        if (!mbar_wait(&o_done[t], (j - 1) & 1, p.err, abort_flag, 17)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const float mb = -m_use;
 #pragma unroll
       for (int c8 = 0; c8 < ATT_BKV / 8; ++c8) {
-        uint32_t w[4];
+        uint32_t w4[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float p0 = ex2_approx(s[c8 * 8 + 2 * i] - m_new);
-          const float p1 = ex2_approx(s[c8 * 8 + 2 * i + 1] - m_new);
-          sum += p0 + p1;
-          w[i] = pack_bf16(p0, p1);
+          const float x0 = fmaf(s[c8 * 8 + 2 * i], c, mb);
+          const float x1 = fmaf(s[c8 * 8 + 2 * i + 1], c, mb);
+          w4[i] = ex2_f16x2(pack_f16(x0, x1));
         }
         const int half = c8 >> 3, chunk = c8 & 7;
         uint8_t* dst = pbuf + half * (ATT_BQ * 128) + r * 128 + ((chunk ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      l_run = l_run * alpha + sum;
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {   // the scores are dead here: registers are free
+        float v[32], w[16];
+        tmem_ld32(o_tm, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+        tmem_st32(o_tm, v);
+        tmem_ld32(o_tm + 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+        tmem_st32(o_tm + 32, v);
+        tmem_ld16(o_tm + 64, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] *= alpha;
+        tmem_st16(o_tm + 64, w);
+        tmem_st_wait();
+      }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    if (ok && nkv >= 2) ok = consume_o(nkv - 2);
-    if (ok) ok = consume_o(nkv - 1);
-    if (ok) {
-      const int q = q0 + r;
+    if (ok && mbar_wait(&o_done[t], (nkv - 1) & 1, p.err, abort_flag, 18)) {
+      tc_fence_after();
+      float o[64], w[16];
+      float v[32];
+      tmem_ld32(o_tm, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = v[i];
+      tmem_ld32(o_tm + 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[32 + i] = v[i];
+      tmem_ld16(o_tm + 64, w);
+      tmem_ld_wait();
+      const int q = q0 + t * ATT_BQ + r;
       if (q < p.T) {
-        const float inv = 1.0f / l_run;
+        const float inv = 1.0f / w[0];
         uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.T + q) * p.d + h * ATT_HD);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          dst[j] = make_uint4(pack_bf16(o_acc[8 * j + 0] * inv, o_acc[8 * j + 1] * inv),
-                              pack_bf16(o_acc[8 * j + 2] * inv, o_acc[8 * j + 3] * inv),
-                              pack_bf16(o_acc[8 * j + 4] * inv, o_acc[8 * j + 5] * inv),
-                              pack_bf16(o_acc[8 * j + 6] * inv, o_acc[8 * j + 7] * inv));
+        for (int k = 0; k < 8; ++k) {
+          dst[k] = make_uint4(pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv),
+                              pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                              pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                              pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
         }
       }
     }

@@ -259,9 +259,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const int gb = m / p.vt_T, t = m % p.vt_T;
               const int h = col >> 6, e0 = col & 63;
               const int H = (p.N - p.vt_col0) >> 6;
-              __nv_bfloat16* dst = p.vt + (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
+              __half* dst = p.vt + (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) dst[static_cast<long long>(i) * p.vt_ld] = __float2bfloat16_rn(v[c][i]);
+              for (int i = 0; i < 32; ++i)   // f16 for the attention's f16 P.V product (saturated to its range)
+                dst[static_cast<long long>(i) * p.vt_ld] = __float2half_rn(fminf(fmaxf(v[c][i], -65504.0f), 65504.0f));
             }
             continue;
           }

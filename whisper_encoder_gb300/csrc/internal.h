@@ -42,8 +42,8 @@ cudaError_t launch_quantize(const __nv_bfloat16* x, long long n, uint8_t* q, con
 cudaError_t launch_finalize_scale(float* amax_to_scale, cudaStream_t s);
 cudaError_t launch_dequantize(const uint8_t* q, const float* scale, long long n, __nv_bfloat16* y,
                               cudaStream_t s);
-cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H,
-                               __nv_bfloat16* vt, cudaStream_t s);
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H, __half* vt,
+                               cudaStream_t s);
 cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long batch_stride_elems,
                              int batch, int row, cudaStream_t s);
 

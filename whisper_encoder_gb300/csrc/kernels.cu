@@ -398,9 +398,9 @@ __global__ void dequantize_kernel(const uint8_t* __restrict__ q, const float* __
   }
 }
 
-// v [batch*T][ld] (head h at columns 64h..64h+63) -> vt [(b*H + h)*64 + e][T_PAD]
+// v [batch*T][ld] (head h at columns 64h..64h+63) -> f16 vt [(b*H + h)*64 + e][T_PAD]
 __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, long long ld, int T, int H,
-                                   __nv_bfloat16* __restrict__ vt) {
+                                   __half* __restrict__ vt) {
   __shared__ __nv_bfloat16 tile[32][34];
   const int b = blockIdx.z;
   const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;  // c over H*64 columns
@@ -413,7 +413,7 @@ __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, long lon
   for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
     const int c = c0 + ty, t = t0 + threadIdx.x;
     const int h = c >> 6, e = c & 63;
-    if (t < T) vt[(static_cast<long long>(b * H + h) * 64 + e) * T_PAD + t] = tile[threadIdx.x][ty];
+    if (t < T) vt[(static_cast<long long>(b * H + h) * 64 + e) * T_PAD + t] = __float2half_rn(__bfloat162float(tile[threadIdx.x][ty]));
   }
 }
 
@@ -541,7 +541,7 @@ cudaError_t launch_dequantize(const uint8_t* q, const float* scale, long long n,
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H, __nv_bfloat16* vt,
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H, __half* vt,
                                cudaStream_t s) {
   dim3 grid((T + 31) / 32, H * 2, batch);
   transpose_v_kernel<<<grid, dim3(32, 8), 0, s>>>(v, ld, T, H, vt);

@@ -2,6 +2,7 @@
 // tensor-core kernels (no device code here).
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace wb {
@@ -47,8 +48,8 @@ struct GemmParams {
   int rows_per_item;         // rows of one batch item (chunk) in the flattened row index
   int act_gelu;              // EPI_BIAS_RESID only: GELU before the residual add
   float* amax;               // if set: per-item atomic max of |y| (feeds the next E4M3 operand's scale)
-  // QKV: columns >= vt_col0 are written transposed to vt[(b*H + h)*64 + e][t]
-  __nv_bfloat16* vt;
+  // QKV: columns >= vt_col0 are written transposed, as f16, to vt[(b*H + h)*64 + e][t]
+  __half* vt;
   int vt_col0, vt_T, vt_ld;  // tokens per batch item, elements between vt rows
   // ---- DFT power epilogue: P split into hi/lo bf16 parts ----
   __nv_bfloat16* pw;         // [batch][2][M][pw_ld]
@@ -60,22 +61,25 @@ struct GemmParams {
   uint32_t* err;
 };
 
-constexpr int ATT_BQ = 128;
-constexpr int ATT_BKV = 128;
-constexpr int ATT_HD = 64;
+constexpr int ATT_BQ = 128;           // queries per tile; a CTA owns two tiles
+constexpr int ATT_TILES = 2;
+constexpr int ATT_BKV = 128;          // keys per step
+constexpr int ATT_HD = 64;            // head dim
+constexpr int ATT_NPV = 80;           // PV MMA width: 64 value columns + 16 columns of ones (row sums)
 constexpr int ATT_STAGES = 3;
-constexpr int ATT_THREADS = 192;
+constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_TILES;   // producer + MMA + one softmax warpgroup per tile
 
 struct AttnSmem {
-  static constexpr int Q_BYTES = ATT_BQ * 128;        // [128 q][64 e] bf16
-  static constexpr int K_BYTES = ATT_BKV * 128;       // [128 kv][64 e]
-  static constexpr int V_BYTES = 2 * ATT_HD * 128;    // 2 halves of [64 e][64 kv]
-  static constexpr int P_BYTES = 2 * ATT_BQ * 128;    // 2 halves of [128 q][64 kv]
+  static constexpr int Q_BYTES = ATT_BQ * 128;              // [128 q][64 e] bf16
+  static constexpr int K_BYTES = ATT_BKV * 128;             // [128 kv][64 e] bf16
+  static constexpr int VH_BYTES = ATT_NPV * 128;            // one V^T half: [64 e][64 kv] f16 + 16 rows of ones
+  static constexpr int V_BYTES = 2 * VH_BYTES;
+  static constexpr int P_BYTES = 2 * ATT_BQ * 128;          // 2 halves of [128 q][64 kv] f16
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + ATT_TILES * Q_BYTES;
   static constexpr int OFF_V = OFF_K + ATT_STAGES * K_BYTES;
   static constexpr int OFF_P = OFF_V + ATT_STAGES * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_P + ATT_TILES * P_BYTES;
   static constexpr int TOTAL = 1024 + OFF_BAR + 256;
 };
 
