@@ -231,6 +231,12 @@ def run_case(args) -> None:
         q, k_, v = rnd(B, 1500, d), rnd(B, 1500, d), rnd(B, 1500, d)
         fn = lambda: wb.attention(q, k_, v, H)  # noqa: E731
         flops = 4.0 * B * H * 1500 * 1500 * 64
+    elif args.case == "layernorm":
+        x = rnd(M, d)
+        gam = torch.ones(d, device="cuda")
+        bet = torch.zeros(d, device="cuda")
+        fn = lambda: wb.layernorm(x, gam, bet)  # noqa: E731
+        flops = 2.0 * M * d * 2      # bytes moved (read + write), reported in the same field
     elif args.case == "logmel":
         audio = torch.randn(B * 480000, device="cuda", generator=g) * 0.1
         fn = lambda: wb.logmel(audio, B, dims.n_mels)  # noqa: E731
@@ -246,8 +252,9 @@ def run_case(args) -> None:
     ev[1].record()
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / 3
+    rate = flops / (ms / 1000)
     print(json.dumps({"case": args.case, "batch": B, "ms": round(ms, 4),
-                      "tflops": round(flops / (ms / 1000) / 1e12, 1)}))
+                      ("gbs" if args.case == "layernorm" else "tflops"): round(rate / (1e9 if args.case == "layernorm" else 1e12), 1)}))
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -260,7 +267,7 @@ def main() -> None:
     ap.add_argument("--precision", choices=("bf16", "mixed_fp8"), default="bf16")
     ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "logmel"), default=None,
+    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "logmel"), default=None,
                     help="launch one kernel class at full size (for profiler captures) instead of the bench")
     args = ap.parse_args()
     if args.case:

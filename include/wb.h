@@ -206,7 +206,7 @@ wb_status wb_linear(const void* a, const void* w, int M, int N, int K, int dtype
  * layernorm_fused / layernorm_fused_residual): total = x + residual,
  * y = (total - mean) / sqrt(var + eps) * g + b over rows of width d (biased
  * variance).  residual and total may be NULL.  x, residual, total, y: bf16
- * [rows, d]; g, b: float32 [d].  d must be a multiple of 128 and <= 2048. */
+ * [rows, d]; g, b: float32 [d], 16-byte aligned.  d must be a multiple of 128 and <= 2048. */
 wb_status wb_layernorm(const void* x, const void* residual, const float* g, const float* b, int rows, int d,
                        float eps, void* y, void* total, void* stream);
 

@@ -732,7 +732,7 @@ wb_status wb_layernorm(const void* x, const void* residual, const float* g, cons
                        float eps, void* y, void* total, void* stream) {
   if (rows < 0 || d < 128 || d > 2048 || d % 128 != 0 || !(eps > 0.0f)) return WB_EINVAL;
   if (rows == 0) return WB_OK;
-  if (!x || !g || !b || !y || !aligned16(x) || !aligned16(y)) return WB_EINVAL;
+  if (!x || !g || !b || !y || !aligned16(x) || !aligned16(y) || !aligned16(g) || !aligned16(b)) return WB_EINVAL;
   if ((residual && !aligned16(residual)) || (total && (!residual || !aligned16(total)))) return WB_EINVAL;
   WB_CUDA(launch_layernorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(residual), g, b,
                            rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total), nullptr, 0,

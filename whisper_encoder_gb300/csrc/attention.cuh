@@ -183,13 +183,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int i = 0; i < 32; ++i) s[q * 32 + i] = v[i];
       }
       tmem_ld_wait();
-      const int valid = min(ATT_BKV, p.T - j * ATT_BKV);
-      float mx = -INFINITY;
+      const int valid = p.T - j * ATT_BKV;
+      if (valid < ATT_BKV) {   // only the last key tile reaches past the sequence end
 #pragma unroll
-      for (int i = 0; i < ATT_BKV; ++i) {
-        s[i] = (i < valid) ? s[i] : -INFINITY;
-        mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < ATT_BKV; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
       }
+      float m4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m4[k] = fmaxf(s[2 * k], s[2 * k + 1]);       // s[0..7]
+#pragma unroll
+      for (int i = 8; i < ATT_BKV; i += 8) {                                     // s[8..127], 8 per step
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
+      }
+      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
       const float m_cand = mx * c;
       float alpha = 1.0f;
       bool rescale = false;

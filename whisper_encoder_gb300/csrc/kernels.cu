@@ -173,100 +173,124 @@ struct VecIO<4> {
 
 constexpr int LN_WARPS = 8;
 
-// amax (optional): per-item absmax of the bf16 outputs, item = row / rows_per_item.
-template <int NV, int VEC>
-__global__ void layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
-                                 const float* __restrict__ g, const float* __restrict__ bta, int rows, float eps,
-                                 __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ total,
-                                 float* __restrict__ amax, int rows_per_item) {
+template <int NV, int VEC, bool RES>
+__device__ __forceinline__ void ln_load(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
+                                        long long row, int lane, typename VecIO<VEC>::T (&u)[NV],
+                                        typename VecIO<VEC>::T (&ur)[NV]) {
+  using V = typename VecIO<VEC>::T;
+  constexpr int D = NV * VEC * 32;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    u[i] = __ldg(reinterpret_cast<const V*>(x + row * D + (i * 32 + lane) * VEC));
+    if (RES) ur[i] = __ldg(reinterpret_cast<const V*>(res + row * D + (i * 32 + lane) * VEC));
+  }
+}
+
+// Persistent: warp w normalises the contiguous rows [w*R, (w+1)*R), loading row i+1 before it
+// reduces row i so that two rows of loads are in flight per warp.  amax (optional): per-item
+// absmax of the bf16 outputs, item = row / rows_per_item, one atomic per warp and item.
+template <int NV, int VEC, bool RES>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
+                     const float* __restrict__ g, const float* __restrict__ bta, int rows, float eps,
+                     __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ total, float* __restrict__ amax,
+                     int rows_per_item) {
   constexpr int D = NV * VEC * 32;
   using V = typename VecIO<VEC>::T;
-  __shared__ float w_max[LN_WARPS];
   const int lane = threadIdx.x & 31;
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (row >= rows) {
-    if (amax) {
-      if (lane == 0) w_max[threadIdx.x >> 5] = 0.0f;
-      __syncthreads();
-    }
-    return;
-  }
-  float v[NV * VEC];
+  const long long warp_g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const long long per = (rows + n_warps - 1) / n_warps;
+  const long long r0 = warp_g * per;
+  const long long r1 = r0 + per < rows ? r0 + per : rows;
+  V u[NV], ur[NV], nu[NV], nur[NV];
+  if (r0 < r1) ln_load<NV, VEC, RES>(x, res, r0, lane, u, ur);
+  float run_max = 0.0f;
+  int run_item = r0 < r1 ? static_cast<int>(r0 / rows_per_item) : 0;
+  for (long long row = r0; row < r1; ++row) {
+    if (row + 1 < r1) ln_load<NV, VEC, RES>(x, res, row + 1, lane, nu, nur);
+    float v[NV * VEC];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int off = (i * 32 + lane) * VEC;
-    V u = *reinterpret_cast<const V*>(x + row * D + off);
-    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+    for (int i = 0; i < NV; ++i) {
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u[i]);
 #pragma unroll
-    for (int j = 0; j < VEC; ++j) v[i * VEC + j] = __bfloat162float(h[j]);
-    if (res) {
-      V r = *reinterpret_cast<const V*>(res + row * D + off);
-      const __nv_bfloat16* hr = reinterpret_cast<const __nv_bfloat16*>(&r);
+      for (int j = 0; j < VEC; ++j) v[i * VEC + j] = __bfloat162float(h[j]);
+      if (RES) {
+        const __nv_bfloat16* hr = reinterpret_cast<const __nv_bfloat16*>(&ur[i]);
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) v[i * VEC + j] += __bfloat162float(hr[j]);
-      if (total) {
-        V o;
-        uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+        for (int j = 0; j < VEC; ++j) v[i * VEC + j] += __bfloat162float(hr[j]);
+        if (total) {
+          V o;
+          uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-        for (int j = 0; j < VEC / 2; ++j) o32[j] = pack_bf16(v[i * VEC + 2 * j], v[i * VEC + 2 * j + 1]);
-        *reinterpret_cast<V*>(total + row * D + off) = o;
-      }
-    }
-  }
-  float s = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NV * VEC; ++i) s += v[i];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const float mean = s * (1.0f / D);
-  float q = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NV * VEC; ++i) {
-    const float t = v[i] - mean;
-    q += t * t;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-  const float rstd = rsqrtf(q * (1.0f / D) + eps);
-  float mx = 0.0f;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int off = (i * 32 + lane) * VEC;
-    V o;
-    uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-    for (int j = 0; j < VEC / 2; ++j) {
-      const float y0 = (v[i * VEC + 2 * j] - mean) * rstd * __ldg(g + off + 2 * j) + __ldg(bta + off + 2 * j);
-      const float y1 =
-          (v[i * VEC + 2 * j + 1] - mean) * rstd * __ldg(g + off + 2 * j + 1) + __ldg(bta + off + 2 * j + 1);
-      o32[j] = pack_bf16(y0, y1);
-      if (amax) {
-        const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&o32[j]);
-        mx = fmaxf(mx, fmaxf(fabsf(__bfloat162float(hv.x)), fabsf(__bfloat162float(hv.y))));
-      }
-    }
-    *reinterpret_cast<V*>(y + row * D + off) = o;
-  }
-  if (amax) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) w_max[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {   // the block's 8 rows span at most two items: merge, then 1-2 atomics
-      const long long row0 = static_cast<long long>(blockIdx.x) * LN_WARPS;
-      int cur = static_cast<int>(row0 / rows_per_item);
-      float m = 0.0f;
-      for (int w = 0; w < LN_WARPS && row0 + w < rows; ++w) {
-        const int it = static_cast<int>((row0 + w) / rows_per_item);
-        if (it != cur) {
-          if (m > 0.0f) atomic_max_nonneg(amax + cur, m);
-          cur = it;
-          m = 0.0f;
+          for (int j = 0; j < VEC / 2; ++j) o32[j] = pack_bf16(v[i * VEC + 2 * j], v[i * VEC + 2 * j + 1]);
+          *reinterpret_cast<V*>(total + row * D + (i * 32 + lane) * VEC) = o;
         }
-        m = fmaxf(m, w_max[w]);
       }
-      if (m > 0.0f) atomic_max_nonneg(amax + cur, m);
     }
+    float sm = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV * VEC; ++i) sm += v[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    const float mean = sm * (1.0f / D);
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV * VEC; ++i) {
+      const float t = v[i] - mean;
+      q += t * t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float rstd = rsqrtf(q * (1.0f / D) + eps);
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int off = (i * 32 + lane) * VEC;
+      // gamma / beta for this lane's VEC columns as 16-byte vector loads (L1-resident, coalesced)
+      float gg[VEC], bb[VEC];
+#pragma unroll
+      for (int j4 = 0; j4 < VEC / 4; ++j4) {
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + off) + j4);
+        const float4 b4 = __ldg(reinterpret_cast<const float4*>(bta + off) + j4);
+        gg[4 * j4 + 0] = g4.x; gg[4 * j4 + 1] = g4.y; gg[4 * j4 + 2] = g4.z; gg[4 * j4 + 3] = g4.w;
+        bb[4 * j4 + 0] = b4.x; bb[4 * j4 + 1] = b4.y; bb[4 * j4 + 2] = b4.z; bb[4 * j4 + 3] = b4.w;
+      }
+      V o;
+      uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < VEC / 2; ++j) {
+        const float y0 = (v[i * VEC + 2 * j] - mean) * rstd * gg[2 * j] + bb[2 * j];
+        const float y1 = (v[i * VEC + 2 * j + 1] - mean) * rstd * gg[2 * j + 1] + bb[2 * j + 1];
+        o32[j] = pack_bf16(y0, y1);
+        if (amax) {
+          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&o32[j]);
+          mx = fmaxf(mx, fmaxf(fabsf(__bfloat162float(hv.x)), fabsf(__bfloat162float(hv.y))));
+        }
+      }
+      *reinterpret_cast<V*>(y + row * D + off) = o;
+    }
+    if (amax) {
+      const int item = static_cast<int>(row / rows_per_item);
+      if (item != run_item) {     // rows are contiguous per warp: items change rarely
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) run_max = fmaxf(run_max, __shfl_xor_sync(0xffffffffu, run_max, o));
+        if (lane == 0 && run_max > 0.0f) atomic_max_nonneg(amax + run_item, run_max);
+        run_max = 0.0f;
+        run_item = item;
+      }
+      run_max = fmaxf(run_max, mx);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      u[i] = nu[i];
+      if (RES) ur[i] = nur[i];
+    }
+  }
+  if (amax && r0 < r1) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) run_max = fmaxf(run_max, __shfl_xor_sync(0xffffffffu, run_max, o));
+    if (lane == 0 && run_max > 0.0f) atomic_max_nonneg(amax + run_item, run_max);
   }
 }
 
@@ -472,8 +496,16 @@ template <int NV, int VEC>
 static cudaError_t ln_launch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
                              int rows, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
                              int rows_per_item, cudaStream_t s) {
-  layernorm_kernel<NV, VEC><<<(rows + LN_WARPS - 1) / LN_WARPS, LN_WARPS * 32, 0, s>>>(
-      x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
+  // persistent grid: 2 blocks of 8 warps per SM, each warp walking a contiguous range of rows
+  long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
+  const long long cap = 2LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  if (res)
+    layernorm_kernel<NV, VEC, true><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
+        x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
+  else
+    layernorm_kernel<NV, VEC, false><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
+        x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
   return cudaGetLastError();
 }
 
