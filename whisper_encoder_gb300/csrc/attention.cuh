@@ -4,14 +4,15 @@
 // and "Impact" ("Attention without the quadratic write"): online softmax over
 // key tiles, scores never written to HBM.  Rebuilt on tcgen05:
 //   S_t = Q_t K_j^T        -> TMEM, fp32, one 128-column buffer per query tile
-//   P_t = 2^(S_t c - m_t)  -> f16 in shared memory (packed ex2: two exponentials per MUFU op)
+//   P_t = 2^(S_t c - m_t)  -> f16, written back over S_t in TMEM (packed ex2: two
+//                             exponentials per MUFU op); the PV MMA reads its A operand from TMEM
 //   O_t += P_t [V_j | 1]   -> TMEM, fp32, 80 columns: 64 of output and 16 copies of the
 //                             row sum (a block of ones appended to V^T in shared memory)
 // A CTA owns two 128-query tiles of one (batch, head).  Warp 0 lane 0 loads
 // both Q tiles once and a ring of K / V^T tiles with TMA; warp 1 lane 0 issues
 // the MMAs, alternating between the tiles so that one tile's matrix products
-// run while the other tile's softmax runs; warps 2-5 and 6-9 own one query
-// row per thread of tile 0 and tile 1.  The running max m_t is only moved
+// run while the other tile's softmax runs; warps 2-17 split each query row of
+// the two tiles over two threads (64 score columns each).  The running max m_t is only moved
 // (and O rescaled in TMEM) when a new row maximum exceeds it by more than a
 // factor 2^8, which keeps every P entry below 256.  Keys past the sequence
 // end are masked to -inf; rows past it are not stored.
@@ -41,7 +42,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint64_t* s_full = kv_empty + ATT_STAGES;      // [TILES]
   uint64_t* p_full = s_full + ATT_TILES;         // [TILES]
   uint64_t* o_done = p_full + ATT_TILES;         // [TILES]
-  uint64_t* mma_done = o_done + ATT_TILES;
+  uint64_t* xbar = o_done + ATT_TILES;           // [TILES][4]: row-max exchange between the two row halves
+  uint64_t* mma_done = xbar + ATT_TILES * 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -62,8 +64,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     for (int t = 0; t < ATT_TILES; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 4);
+      mbar_init(&p_full[t], 4 * ATT_HALVES);
       mbar_init(&o_done[t], 1);
+      for (int q = 0; q < 4; ++q) mbar_init(&xbar[t * 4 + q], ATT_HALVES);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -119,14 +122,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       auto pv = [&](int t, int jj) {
-        const uint32_t sp = smem_u32(smem + S::OFF_P + t * S::P_BYTES);
+        // P_t sits in the first 64 columns of S_t (two f16 per column): 8 columns per K16 step
         const uint32_t sv = smem_u32(smem + S::OFF_V + (jj % ATT_STAGES) * S::V_BYTES);
         const uint32_t o_tm = tmem + 256 + t * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k & 3) * 32;
-          mma_bf16(o_tm, sw128_desc(sp + (k >> 2) * (ATT_BQ * 128) + off),
-                   sw128_desc(sv + (k >> 2) * S::VH_BYTES + off), IDESC_O, (jj | k) != 0);
+          mma_f16_tmem_a(o_tm, tmem + t * 128 + k * 8, sw128_desc(sv + (k >> 2) * S::VH_BYTES + off), IDESC_O,
+                         (jj | k) != 0);
         }
         mma_commit(&o_done[t]);
       };
@@ -160,13 +163,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else {
     // --------------------------- softmax / output --------------------------
-    const int t = (warp - 2) >> 2;                 // query tile of this warpgroup
+    // 16 warps: tile t = sw / 8, row half hf = (sw / 4) % 2 (score columns 64 hf .. 64 hf + 63),
+    // TMEM lane quarter = warp % 4.  The two threads holding the halves of one row exchange
+    // their half-row maxima through shared memory (one mbarrier per tile and lane quarter).
+    const int sw = warp - 2;
+    const int t = sw >> 3;
+    const int hf = (sw >> 2) & 1;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;             // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + t * 128;
+    const uint32_t s_tm = tmem + lane_off + t * 128 + hf * 64;
     const uint32_t o_tm = tmem + lane_off + 256 + t * 128;
-    uint8_t* pbuf = smem + S::OFF_P + t * S::P_BYTES;
+    const uint32_t p_tm = tmem + lane_off + t * 128 + hf * 32;   // this half's 32 packed P columns
+    float* xmax = reinterpret_cast<float*>(smem + S::OFF_XMAX);
+    uint64_t* xb = &xbar[t * 4 + quarter];
     const float c = p.scale_log2;
     float m_use = -INFINITY;
     bool ok = true;
@@ -174,29 +184,39 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     for (int j = 0; j < nkv && ok; ++j) {
       if (!mbar_wait(&s_full[t], j & 1, p.err, abort_flag, 16)) { ok = false; break; }
       tc_fence_after();
-      float s[ATT_BKV];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      float s[64];
+      {
         float v[32];
-        tmem_ld32(s_tm + q * 32, v);
+        tmem_ld32(s_tm, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[q * 32 + i] = v[i];
+        for (int i = 0; i < 32; ++i) s[i] = v[i];
+        tmem_ld32(s_tm + 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
       }
       tmem_ld_wait();
-      const int valid = p.T - j * ATT_BKV;
-      if (valid < ATT_BKV) {   // only the last key tile reaches past the sequence end
+      const int valid = p.T - j * ATT_BKV - hf * 64;      // columns of this half inside the sequence
+      if (valid < 64) {
 #pragma unroll
-        for (int i = 0; i < ATT_BKV; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
+        for (int i = 0; i < 64; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
       }
       float m4[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) m4[k] = fmaxf(s[2 * k], s[2 * k + 1]);       // s[0..7]
 #pragma unroll
-      for (int i = 8; i < ATT_BKV; i += 8) {                                     // s[8..127], 8 per step
+      for (int i = 8; i < 64; i += 8) {                                          // s[8..63], 8 per step
 #pragma unroll
         for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
       }
-      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+      const float own = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+      float* xm = xmax + ((j & 1) * ATT_TILES + t) * ATT_HALVES * ATT_BQ;
+      xm[hf * ATT_BQ + r] = own;
+      tc_fence_before();           // this half's TMEM loads of S precede the partner's P stores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xb);
+      if (!mbar_wait(xb, j & 1, p.err, abort_flag, 19)) { ok = false; break; }
+      tc_fence_after();
+      const float mx = fmaxf(own, xm[(1 - hf) * ATT_BQ + r]);
       const float m_cand = mx * c;
       float alpha = 1.0f;
       bool rescale = false;
@@ -213,61 +233,47 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tc_fence_after();
       }
       const float mb = -m_use;
+      uint32_t pw[32];
 #pragma unroll
-      for (int c8 = 0; c8 < ATT_BKV / 8; ++c8) {
-        uint32_t w4[4];
+      for (int i = 0; i < 32; ++i) pw[i] = ex2_f16x2(pack_f16(fmaf(s[2 * i], c, mb), fmaf(s[2 * i + 1], c, mb)));
+      // Half 1's P columns (32..63) overlay half 0's scores; half 0 finished reading them before
+      // it arrived at the row-max exchange, which half 1 has passed.
+      tmem_st32u(p_tm, pw);
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        // half 0 rescales O columns 0..31 and the row sums 64..79, half 1 columns 32..63
+        float v[32];
+        tmem_ld32(o_tm + hf * 32, v);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x0 = fmaf(s[c8 * 8 + 2 * i], c, mb);
-          const float x1 = fmaf(s[c8 * 8 + 2 * i + 1], c, mb);
-          w4[i] = ex2_f16x2(pack_f16(x0, x1));
+        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+        tmem_st32(o_tm + hf * 32, v);
+        if (hf == 0) {
+          float w[16];
+          tmem_ld16(o_tm + 64, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] *= alpha;
+          tmem_st16(o_tm + 64, w);
         }
-        const int half = c8 >> 3, chunk = c8 & 7;
-        uint8_t* dst = pbuf + half * (ATT_BQ * 128) + r * 128 + ((chunk ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {   // the scores are dead here: registers are free
-        float v[32], w[16];
-        tmem_ld32(o_tm, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(o_tm, v);
-        tmem_ld32(o_tm + 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(o_tm + 32, v);
-        tmem_ld16(o_tm + 64, w);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] *= alpha;
-        tmem_st16(o_tm + 64, w);
         tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
     if (ok && mbar_wait(&o_done[t], (nkv - 1) & 1, p.err, abort_flag, 18)) {
       tc_fence_after();
-      float o[64], w[16];
-      float v[32];
-      tmem_ld32(o_tm, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = v[i];
-      tmem_ld32(o_tm + 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[32 + i] = v[i];
+      float o[32], w[16];
+      tmem_ld32(o_tm + hf * 32, o);
       tmem_ld16(o_tm + 64, w);
       tmem_ld_wait();
       const int q = q0 + t * ATT_BQ + r;
       if (q < p.T) {
         const float inv = 1.0f / w[0];
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.T + q) * p.d + h * ATT_HD);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.T + q) * p.d + h * ATT_HD + hf * 32);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           dst[k] = make_uint4(pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv),
                               pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
                               pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv),

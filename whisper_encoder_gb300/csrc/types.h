@@ -66,20 +66,20 @@ constexpr int ATT_TILES = 2;
 constexpr int ATT_BKV = 128;          // keys per step
 constexpr int ATT_HD = 64;            // head dim
 constexpr int ATT_NPV = 80;           // PV MMA width: 64 value columns + 16 columns of ones (row sums)
-constexpr int ATT_STAGES = 3;
-constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_TILES;   // producer + MMA + one softmax warpgroup per tile
+constexpr int ATT_STAGES = 5;
+constexpr int ATT_HALVES = 2;         // each score row is split over two softmax threads (64 columns each)
+constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_TILES * ATT_HALVES;   // producer + MMA + softmax warps
 
 struct AttnSmem {
   static constexpr int Q_BYTES = ATT_BQ * 128;              // [128 q][64 e] bf16
   static constexpr int K_BYTES = ATT_BKV * 128;             // [128 kv][64 e] bf16
   static constexpr int VH_BYTES = ATT_NPV * 128;            // one V^T half: [64 e][64 kv] f16 + 16 rows of ones
   static constexpr int V_BYTES = 2 * VH_BYTES;
-  static constexpr int P_BYTES = 2 * ATT_BQ * 128;          // 2 halves of [128 q][64 kv] f16
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + ATT_TILES * Q_BYTES;
   static constexpr int OFF_V = OFF_K + ATT_STAGES * K_BYTES;
-  static constexpr int OFF_P = OFF_V + ATT_STAGES * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + ATT_TILES * P_BYTES;
+  static constexpr int OFF_XMAX = OFF_V + ATT_STAGES * V_BYTES;             // [2 parity][tile][half][128] f32
+  static constexpr int OFF_BAR = OFF_XMAX + 2 * ATT_TILES * ATT_HALVES * ATT_BQ * 4;
   static constexpr int TOTAL = 1024 + OFF_BAR + 256;
 };
 
