@@ -63,6 +63,11 @@ def bytes_per_chunk(dims) -> dict:
     return {"enc.layernorm": (2 * L + 1) * T * d * 2 * 2.0}
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture of the
+# kernel class at the batch-32 shape (profiles/); None where the code changed since the capture.
+TRAFFIC = {"enc.attention": 472.2e6}
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -267,6 +272,7 @@ def main() -> None:
     ap.add_argument("--precision", choices=("bf16", "mixed_fp8"), default="bf16")
     ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph of the three calls")
     ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "logmel"), default=None,
                     help="launch one kernel class at full size (for profiler captures) instead of the bench")
     args = ap.parse_args()
@@ -308,8 +314,17 @@ def main() -> None:
     pipe = wb.Pipeline(dims, stem, enc, B, precision)
     stream = torch.cuda.current_stream()
 
-    for _ in range(args.warmup):
+    step = (lambda: pipe(audio))  # noqa: E731
+    graph_launches = None
+    if args.graph:
+        wb.profile_begin()                       # count the library's launches in one eager step
         pipe(audio)
+        torch.cuda.synchronize()
+        graph_launches = sum(n for _, n in wb.profile_end().values())
+        graph = pipe.capture(audio)
+        step = graph.replay
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
     if wb.check_device_error() != 0:
         raise RuntimeError("device error during warm-up")
@@ -322,14 +337,15 @@ def main() -> None:
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    wb.profile_begin()
+    if not args.graph:
+        wb.profile_begin()
     for k in range(args.steps):
         flush.zero_()
         starts[k].record(stream)
-        pipe(audio)
+        step()
         stops[k].record(stream)
     torch.cuda.synchronize()
-    prof = wb.profile_end()
+    prof = wb.profile_end() if not args.graph else {}
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
@@ -359,7 +375,7 @@ def main() -> None:
     e_start.record(stream)
     for _ in range(args.steps):
         audio.copy_(audio_host, non_blocking=True)
-        pipe(audio)
+        step()
         out_host.copy_(pipe.out, non_blocking=True)
     e_stop.record(stream)
     torch.cuda.synchronize()
@@ -380,18 +396,22 @@ def main() -> None:
             kernels[name]["tflops"] = round(fl[name] * B / (per_step_ms / 1000.0) / 1e12, 1)
     fp8_classes = {"enc.qkv", "enc.fc1", "enc.fc2"} if args.precision == "mixed_fp8" else set()
     tensor_classes = [c for c in prof if c in fl]
-    dom = max(tensor_classes, key=lambda c: prof[c][0])
-    dom_ms, dom_n = prof[dom]
-    per_launch_ms = dom_ms / dom_n
-    flops_launch = fl[dom] * B / (dom_n / args.steps)
-    achieved = flops_launch / (per_launch_ms / 1000.0) / 1e12
-    peak = peaks["bf16_sustained"] * (2.0 if dom in fp8_classes else 1.0)
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
-                "flops_per_launch": flops_launch, "ms_per_launch": round(per_launch_ms, 4),
-                "peak_source": f"{peaks['source']} bf16 sustained" + (" x2 (E4M3 nominal ratio)" if dom in fp8_classes else "")}
+    roofline = None
+    if tensor_classes:
+        dom = max(tensor_classes, key=lambda c: prof[c][0])
+        dom_ms, dom_n = prof[dom]
+        per_launch_ms = dom_ms / dom_n
+        flops_launch = fl[dom] * B / (dom_n / args.steps)
+        achieved = flops_launch / (per_launch_ms / 1000.0) / 1e12
+        peak = peaks["bf16_sustained"] * (2.0 if dom in fp8_classes else 1.0)
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(dom),
+                    "flops_per_launch": flops_launch, "ms_per_launch": round(per_launch_ms, 4),
+                    "peak_source": f"{peaks['source']} bf16 sustained"
+                                   + (" x2 (E4M3 nominal ratio)" if dom in fp8_classes else "")}
     step_flops = sum(fl.values()) * B
-    gpu_launches = sum(n for _, n in prof.values())
+    # launches per step: counted by the library's own events (eager), or one graph launch
+    gpu_launches = sum(n for _, n in prof.values()) if prof else graph_launches * args.steps
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -400,7 +420,7 @@ def main() -> None:
         "impl": "wb",
         "config": arm_config(args, world),
         "tflops": round(step_flops / (ms_step / 1000.0) / 1e12, 1),
-        "roofline": roofline, "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks,
+        "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "graph": bool(args.graph),
         "kernels": kernels,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

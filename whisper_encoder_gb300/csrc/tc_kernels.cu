@@ -7,11 +7,40 @@
 
 namespace wb {
 
-int sm_count() {
-  int dev = 0, n = 0;
+namespace {
+
+constexpr int kMaxDev = 64;
+int g_sm_count[kMaxDev] = {0};
+std::mutex g_attr_mu;
+
+int current_device() {
+  int dev = 0;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  return (dev >= 0 && dev < kMaxDev) ? dev : 0;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (so that launches stay free of
+// attribute calls, which keeps them legal inside CUDA-graph stream capture).
+template <typename K>
+cudaError_t ensure_smem_attr(K kern, int smem, uint64_t* done_mask) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (*done_mask & (1ull << dev)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) *done_mask |= 1ull << dev;
+  return e;
+}
+
+}  // namespace
+
+int sm_count() {
+  const int dev = current_device();
+  if (g_sm_count[dev] <= 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = n > 0 ? n : 1;
+  }
+  return g_sm_count[dev];
 }
 
 namespace {
@@ -20,9 +49,8 @@ template <int BN, bool FP8, int EPI>
 cudaError_t gemm_launch_t(const GemmLaunch& g, cudaStream_t s) {
   auto kern = gemm_kernel<BN, FP8, EPI>;
   const int smem = GemmSmem<BN>::TOTAL;
-  // cudaFuncSetAttribute is cheap and idempotent; doing it per call keeps
-  // multi-device processes correct without per-device bookkeeping.
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static uint64_t attr_done = 0;
+  cudaError_t e = ensure_smem_attr(kern, smem, &attr_done);
   if (e != cudaSuccess) return e;
   const int m_tiles = (g.p.M + GEMM_BM - 1) / GEMM_BM;
   const int n_tiles = (g.p.N + BN - 1) / BN;
@@ -63,7 +91,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 cudaError_t launch_attention(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& vt,
                              const AttnParams& p, cudaStream_t s) {
   const int smem = AttnSmem::TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static uint64_t attr_done = 0;
+  cudaError_t e = ensure_smem_attr(attention_kernel, smem, &attr_done);
   if (e != cudaSuccess) return e;
   const int n_qp = (p.T + ATT_TILES * ATT_BQ - 1) / (ATT_TILES * ATT_BQ);
   const long long grid = static_cast<long long>(p.batch) * p.H * n_qp;
