@@ -81,6 +81,12 @@ def layer_norm(x: np.ndarray, g, b, eps: float = LN_EPS) -> np.ndarray:
     return (x - mu) / np.sqrt(var + eps) * np.asarray(g, np.float64) + np.asarray(b, np.float64)
 
 
+def rms_norm(x: np.ndarray, g, eps: float = LN_EPS) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * g over the last axis (the PyPI page, "Direct Kernel API": rmsnorm_fused)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * np.asarray(g, np.float64)
+
+
 def softmax(s: np.ndarray) -> np.ndarray:
     """Row softmax (max subtracted first, which leaves the value unchanged)."""
     s = s - s.max(axis=-1, keepdims=True)
@@ -167,3 +173,16 @@ def forward(chunk: np.ndarray, weights: dict, n_mels: int, n_heads: int, **kw) -
     """Audio chunk [480000] -> encoder output [1500, d] (log-mel, stem, layers, LN_post)."""
     from . import frontend
     return encoder(conv_stem(frontend.log_mel(chunk, n_mels), weights), weights, n_heads, **kw)
+
+
+def cross_kv(enc_out: np.ndarray, layers: list) -> list:
+    """Decoder cross-attention keys and values of the encoder output, one (K, V) pair per decoder layer.
+
+    The showcase site, "The Approach" (decoder_cross_attn site) and "The Solution" (decoder
+    cross-attention is one of the three attention patterns): the decoder attends to the
+    encoder output through its own key / value projections; Whisper's key projection has no
+    bias.  K = enc_out Wk^T, V = enc_out Wv^T + bv, enc_out [T, d].
+    """
+    f64 = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    e = f64(enc_out)
+    return [(e @ f64(L["wk"]).T, e @ f64(L["wv"]).T + f64(L["bv"])) for L in layers]

@@ -94,3 +94,51 @@ def fake_quantize(x) -> np.ndarray:
     """dequantize(quantize(x)): the value an E4M3 operand with one per-tensor scale carries."""
     codes, scale = quantize(np.asarray(x, dtype=np.float32))
     return dequantize(codes, scale)
+
+
+# --- E5M2 ----------------------------------------------------------------------------------------
+# The showcase site, "The Solution" (fp8_quantize.cu card: casts for both E4M3 and E5M2, "more
+# range") and "The Approach" (aggressive_fp8 switches cross-attention activations to E5M2).
+# Format (OCP 8-bit floating point, E5M2): sign, 5 exponent bits with bias 15, 2 mantissa bits;
+# exponent field 0 encodes subnormals m * 2^-16; exponent 31 encodes inf (m = 0) and NaN;
+# the largest finite magnitude is 1.75 * 2^15 = 57344.  Rounding reading as for E4M3: nearest,
+# ties to the even code, magnitudes above 57344 (and infinities) saturate to +-57344.
+
+E5M2_MAX = 57344.0
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 2) & 0x1F
+    m = (c & 0x3).astype(np.float64)
+    val = np.where(e == 0, m / 4.0 * 2.0 ** -14, (1.0 + m / 4.0) * np.exp2(e.astype(np.float64) - 15.0))
+    val = np.where(e == 31, np.where(m == 0, np.inf, np.nan), val)
+    return sign * val
+
+
+_POS_E5M2 = e5m2_decode(np.arange(0x7C))        # finite non-negative values, codes 0x00 .. 0x7B
+
+
+def e5m2_encode(x) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    hi = np.minimum(np.searchsorted(_POS_E5M2, ax, side="left"), len(_POS_E5M2) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = ax - _POS_E5M2[lo]
+    d_hi = _POS_E5M2[hi] - ax
+    code = np.where((d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)), hi, lo)
+    code = np.where(ax >= E5M2_MAX, 0x7B, code)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def quantize_e5m2(x):
+    """Per-tensor E5M2: scale = amax / 57344, code = e5m2(float32(x) * (57344 / amax))."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x32))) if x32.size else np.float32(0)
+    if amax == 0:
+        return e5m2_encode(x32), np.float32(1.0)
+    inv = np.float32(np.float32(E5M2_MAX) / amax)
+    return e5m2_encode((x32 * inv).astype(np.float32)), np.float32(amax / np.float32(E5M2_MAX))

@@ -166,6 +166,17 @@ def encoder_weights(dims: Dims, seed: int, dtype: str = "bf16", n_layers: int | 
     return w
 
 
+def cross_kv_weights(dims: Dims, seed: int, n_layers: int, dtype: str = "bf16") -> list:
+    """Random-init decoder cross-attention projections per decoder layer: wk, wv [d, d], bv [d]."""
+    rng = np.random.default_rng(seed)
+    d = dims.d_model
+    out = []
+    for _ in range(n_layers):
+        out.append({"wk": round_to(_normal(rng, (d, d)), dtype), "wv": round_to(_normal(rng, (d, d)), dtype),
+                    "bv": round_to(_normal(rng, (d,)), dtype)})
+    return out
+
+
 def gemm_operands(seed: int, m: int, n: int, k: int, lo: int = -3, hi: int = 3):
     """Small-integer GEMM operands (exact in bf16 and E4M3), float32 arrays."""
     rng = np.random.default_rng(seed)

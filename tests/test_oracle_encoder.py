@@ -254,3 +254,37 @@ def test_fp8_sites_quantise_off_grid_operands():
     diff = np.abs(oenc.encoder_layer(h, L, H, ("qkv",)) - ref).max()
     assert 1e-6 < diff < 0.1 * np.abs(ref).max()                   # the QKV input was rounded
     assert np.abs(oenc.encoder_layer(h, L, H, ("ffn",)) - ref).max() < 1e-12   # FC1 input on grid, FC2 input 0
+
+
+def test_rms_norm_matches_torch_and_unit_rms():
+    x = np.random.default_rng(12).normal(0.5, 2.0, size=(33, 1280))
+    g = np.random.default_rng(13).normal(size=1280)
+    ref = torch.nn.functional.rms_norm(torch.tensor(x), (1280,), torch.tensor(g), 1e-5).numpy()
+    np.testing.assert_allclose(enc.rms_norm(x, g), ref, atol=1e-12)
+    y = enc.rms_norm(x, np.ones(1280))
+    ms = (x * x).mean(1)
+    np.testing.assert_allclose((y * y).mean(1), ms / (ms + 1e-5), rtol=1e-12)
+
+
+def test_cross_kv_drives_torch_cross_attention():
+    # the oracle's K / V, used as key and value of a softmax attention, reproduce torch's
+    # MultiheadAttention(query, memory, memory) with the same projection weights
+    d, H, T, Tq = 64, 2, 40, 7
+    rng = np.random.default_rng(14)
+    L = {"wk": rng.normal(size=(d, d)) * 0.1, "wv": rng.normal(size=(d, d)) * 0.1, "bv": rng.normal(size=d) * 0.1}
+    wq, bq = rng.normal(size=(d, d)) * 0.1, rng.normal(size=d) * 0.1
+    wo, bo = np.eye(d), np.zeros(d)
+    mem = rng.normal(size=(T, d))
+    query = rng.normal(size=(Tq, d))
+    (k, v), = enc.cross_kv(mem, [L])
+    q = query @ wq.T + bq
+    hd = d // H
+    ours = np.concatenate([enc.softmax(q[:, h * hd:(h + 1) * hd] @ k[:, h * hd:(h + 1) * hd].T / math.sqrt(hd))
+                           @ v[:, h * hd:(h + 1) * hd] for h in range(H)], axis=1) @ wo.T + bo
+    mha = torch.nn.MultiheadAttention(d, H, bias=True, batch_first=True, dtype=torch.float64)
+    with torch.no_grad():
+        mha.in_proj_weight.copy_(torch.tensor(np.concatenate([wq, L["wk"], L["wv"]])))
+        mha.in_proj_bias.copy_(torch.tensor(np.concatenate([bq, np.zeros(d), L["bv"]])))
+        mha.out_proj.weight.copy_(torch.tensor(wo)); mha.out_proj.bias.copy_(torch.tensor(bo))
+    ref = mha(torch.tensor(query)[None], torch.tensor(mem)[None], torch.tensor(mem)[None])[0][0].detach().numpy()
+    np.testing.assert_allclose(ours, ref, atol=1e-12)

@@ -66,3 +66,26 @@ def test_quantize_recipe():
     assert rel[np.abs(x) > 0.2].max() <= 2.0 ** -4 + 1e-6     # 3 mantissa bits: half-ulp <= 1/16
     q0, s0 = fp8.quantize(np.zeros(10, np.float32))
     assert s0 == 1.0 and (q0 == 0).all()
+
+
+def test_e5m2_decode_all_codes_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    got = fp8.e5m2_decode(codes)
+    assert (np.isnan(ref) == np.isnan(got)).all()
+    finite = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[finite], ref[finite])
+    assert fp8.e5m2_decode(0x7B) == 57344.0 and fp8.e5m2_decode(0x7C) == np.inf
+
+
+def test_e5m2_encode_roundtrip_midpoints_and_saturation():
+    codes = np.array([c for c in range(256) if (c & 0x7F) < 0x7C], dtype=np.uint8)
+    np.testing.assert_array_equal(fp8.e5m2_encode(fp8.e5m2_decode(codes)), codes)
+    vals = fp8.e5m2_decode(np.arange(0x7C))
+    for c in range(0x7B):
+        mid = 0.5 * (vals[c] + vals[c + 1])
+        assert fp8.e5m2_encode(mid) == (c if c % 2 == 0 else c + 1)
+    assert (fp8.e5m2_encode(np.array([57344.0, 60000.0, 1e9, np.inf])) == 0x7B).all()
+    x = np.random.default_rng(2).normal(0, 3000, 100000).astype(np.float32)
+    x = x[np.abs(x) < 57000]
+    np.testing.assert_array_equal(fp8.e5m2_encode(x), torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy())
