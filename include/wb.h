@@ -218,6 +218,34 @@ size_t wb_attention_workspace_bytes(int batch, int T, int n_heads);
 wb_status wb_attention(const void* q, const void* k, const void* v, int batch, int T, int n_heads, void* out,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* --- after the encoder: decoder cross-attention keys and values ---------------------
+ * The showcase site, "The Solution" (decoder cross-attention is one of the three
+ * attention patterns) and "The Approach" (decoder_cross_attn site): every decoder
+ * layer projects the encoder output to its own keys and values once per audio
+ * chunk.  For decoder layer l: K_l = enc_out Wk_l^T, V_l = enc_out Wv_l^T + bv_l
+ * (Whisper's key projection has no bias).  w[l].w_kv is bf16 [2d, d] = [Wk_l; Wv_l]
+ * (HF layout), w[l].b_kv float32 [2d] = [0, bv_l].  enc_out: bf16 [batch, 1500, d];
+ * kv: bf16 [n_dec_layers][batch * 1500][2d] with K in columns 0..d-1 and V in d..2d-1. */
+typedef struct {
+  const void* w_kv;
+  const float* b_kv;
+} wb_cross_kv_weights;
+wb_status wb_cross_kv(const void* enc_out, int batch, const wb_dims* dims, int n_dec_layers,
+                      const wb_cross_kv_weights* w, void* kv, void* stream);
+
+/* Fused residual + RMSNorm (PyPI page, "Direct Kernel API": rmsnorm_fused):
+ * total = x + residual, y = total / sqrt(mean(total^2) + eps) * g.  As wb_layernorm
+ * without beta; residual and total may be NULL. */
+wb_status wb_rmsnorm(const void* x, const void* residual, const float* g, int rows, int d, float eps, void* y,
+                     void* total, void* stream);
+
+/* FP8 E5M2 casts with one per-tensor scale (showcase site, "The Solution": casts for both
+ * E4M3 and E5M2, E5M2 for more range): amax = max|x|, code = E5M2(x * 57344 / amax)
+ * rounded to nearest even and saturated to +-57344; *scale (device) = amax / 57344
+ * (1 when amax = 0). */
+wb_status wb_quantize_e5m2(const void* x, int64_t n, uint8_t* q, float* scale, void* stream);
+wb_status wb_dequantize_e5m2(const uint8_t* q, const float* scale, int64_t n, void* y, void* stream);
+
 /* --- kernel timing (benchmarks) -------------------------------------------------
  * Between wb_profile_begin() and wb_profile_end() every kernel that libwb
  * launches is bracketed by two CUDA events recorded on its launch stream.

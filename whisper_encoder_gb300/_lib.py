@@ -39,6 +39,10 @@ class wb_layer_weights(ctypes.Structure):
         "w_fc1", "b_fc1", "s_fc1", "w_fc2", "b_fc2", "s_fc2")]
 
 
+class wb_cross_kv_weights(ctypes.Structure):
+    _fields_ = [("w_kv", c_void), ("b_kv", c_void)]
+
+
 class wb_ln_weights(ctypes.Structure):
     _fields_ = [("g", c_void), ("b", c_void)]
 
@@ -64,6 +68,10 @@ SIGNATURES = {
     "wb_layernorm": (c_int, [c_void, c_void, c_void, c_void, c_int, c_int, c_float, c_void, c_void, c_void]),
     "wb_attention_workspace_bytes": (c_size, [c_int, c_int, c_int]),
     "wb_attention": (c_int, [c_void, c_void, c_void, c_int, c_int, c_int, c_void, c_void, c_size, c_void]),
+    "wb_cross_kv": (c_int, [c_void, c_int, P(wb_dims), c_int, P(wb_cross_kv_weights), c_void, c_void]),
+    "wb_rmsnorm": (c_int, [c_void, c_void, c_void, c_int, c_int, c_float, c_void, c_void, c_void]),
+    "wb_quantize_e5m2": (c_int, [c_void, c_i64, c_void, c_void, c_void]),
+    "wb_dequantize_e5m2": (c_int, [c_void, c_void, c_i64, c_void, c_void]),
     "wb_profile_begin": (c_int, []),
     "wb_profile_end": (c_int, [c_int, P(ctypes.c_char_p), P(ctypes.c_double), P(ctypes.c_int64)]),
 }

@@ -20,6 +20,7 @@ N_TOKENS = 1500
 
 PRESET_BF16 = (WB_BF16,) * 6
 PRESET_MIXED_FP8 = (WB_E4M3, WB_E4M3, WB_BF16, WB_BF16, WB_E4M3, WB_E4M3)   # qkv, out, ffn (w, a)
+PRESET_AGGRESSIVE_FP8 = (WB_E4M3,) * 6                                        # every encoder site in E4M3
 
 
 def _p(t) -> ctypes.c_void_p:
@@ -179,6 +180,46 @@ def attention(q, k, v, n_heads: int, stream=None) -> torch.Tensor:
     ws = _workspace(load().wb_attention_workspace_bytes(batch, T, n_heads), q.device)
     call("wb_attention", _p(q), _p(k), _p(v), batch, T, n_heads, _p(out), _p(ws), ws.numel(), _stream(stream))
     return out
+
+
+def rmsnorm(x, g, eps: float = 1e-5, residual=None, return_total: bool = False, stream=None):
+    _need(x, torch.bfloat16, "x")
+    rows, d = x.reshape(-1, x.shape[-1]).shape
+    y = torch.empty_like(x)
+    total = torch.empty_like(x) if return_total else None
+    call("wb_rmsnorm", _p(x), _p(residual), _p(g), rows, d, eps, _p(y), _p(total), _stream(stream))
+    return (y, total) if return_total else y
+
+
+def quantize_e5m2(x: torch.Tensor, stream=None):
+    _need(x, torch.bfloat16, "x")
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    call("wb_quantize_e5m2", _p(x), x.numel(), _p(q), _p(scale), _stream(stream))
+    return q, scale
+
+
+def dequantize_e5m2(q: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:
+    _need(q, torch.uint8, "q")
+    y = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    call("wb_dequantize_e5m2", _p(q), _p(scale), q.numel(), _p(y), _stream(stream))
+    return y
+
+
+def cross_kv(enc_out: torch.Tensor, dims, layers: list, stream=None) -> torch.Tensor:
+    """Decoder cross-attention K|V of the encoder output for every decoder layer.
+
+    layers: per decoder layer (w_kv bf16 [2d, d], b_kv f32 [2d]); returns bf16 [L, batch*1500, 2d]."""
+    _need(enc_out, torch.bfloat16, "enc_out")
+    batch = enc_out.shape[0]
+    d = dims.d_model
+    kv = torch.empty((len(layers), batch * N_TOKENS, 2 * d), dtype=torch.bfloat16, device=enc_out.device)
+    arr = (_lib.wb_cross_kv_weights * max(1, len(layers)))()
+    for i, (w, b) in enumerate(layers):
+        arr[i] = _lib.wb_cross_kv_weights(w.data_ptr(), b.data_ptr())
+    ds = dims_struct(dims)
+    call("wb_cross_kv", _p(enc_out), batch, ctypes.byref(ds), len(layers), arr, _p(kv), _stream(stream))
+    return kv
 
 
 def profile_begin() -> None:

@@ -760,6 +760,58 @@ wb_status wb_attention(const void* q, const void* k, const void* v, int batch, i
                        n_heads, static_cast<__nv_bfloat16*>(out), s);
 }
 
+// -------------------------- decoder-side / extra building blocks --------------------------
+wb_status wb_rmsnorm(const void* x, const void* residual, const float* g, int rows, int d, float eps, void* y,
+                     void* total, void* stream) {
+  if (rows < 0 || d < 128 || d > 2048 || d % 128 != 0 || !(eps > 0.0f)) return WB_EINVAL;
+  if (rows == 0) return WB_OK;
+  if (!x || !g || !y || !aligned16(x) || !aligned16(y) || !aligned16(g)) return WB_EINVAL;
+  if ((residual && !aligned16(residual)) || (total && (!residual || !aligned16(total)))) return WB_EINVAL;
+  WB_CUDA(launch_rmsnorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(residual), g, rows,
+                         d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total),
+                         static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+wb_status wb_quantize_e5m2(const void* x, int64_t n, uint8_t* q, float* scale, void* stream) {
+  if (n < 0 || !scale) return WB_EINVAL;
+  if (n > 0 && (!x || !q || !aligned16(x))) return WB_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  WB_CUDA(cudaMemsetAsync(scale, 0, sizeof(float), s));
+  if (n > 0) WB_CUDA(launch_amax(xb, n, scale, s));
+  WB_CUDA(launch_quantize_e5m2(xb, n, q, scale, s));
+  return WB_OK;
+}
+
+wb_status wb_dequantize_e5m2(const uint8_t* q, const float* scale, int64_t n, void* y, void* stream) {
+  if (n < 0 || !scale) return WB_EINVAL;
+  if (n == 0) return WB_OK;
+  if (!q || !y) return WB_EINVAL;
+  WB_CUDA(launch_dequantize_e5m2(q, scale, n, static_cast<__nv_bfloat16*>(y), static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+wb_status wb_cross_kv(const void* enc_out, int batch, const wb_dims* dims, int n_dec_layers,
+                      const wb_cross_kv_weights* w, void* kv, void* stream) {
+  if (!dims_ok(dims) || batch < 0 || n_dec_layers < 0) return WB_EINVAL;
+  if (batch == 0 || n_dec_layers == 0) return WB_OK;
+  if (!enc_out || !w || !kv || !aligned16(enc_out) || !aligned16(kv)) return WB_EINVAL;
+  const int D = dims->d_model, M = batch * T_TOK;
+  for (int l = 0; l < n_dec_layers; ++l)
+    if (!w[l].w_kv || !w[l].b_kv || !aligned16(w[l].w_kv)) return WB_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int l = 0; l < n_dec_layers; ++l) {
+    GemmParams p = base_params();
+    p.bias = w[l].b_kv;
+    void* out = static_cast<__nv_bfloat16*>(kv) + static_cast<size_t>(l) * M * 2 * D;
+    const wb_status st = dense_gemm(enc_out, w[l].w_kv, M, 2 * D, D, false, EPI_BIAS, out, 2 * D, 2 * D, nullptr, p,
+                                    s, PC_OTHER);
+    if (st != WB_OK) return st;
+  }
+  return WB_OK;
+}
+
 // -------------------------------- profiling ----------------------------------
 wb_status wb_profile_begin(void) {
   std::lock_guard<std::mutex> lk(g_mu);

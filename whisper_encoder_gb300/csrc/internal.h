@@ -32,6 +32,12 @@ cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16*
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
                              int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
                              int rows_per_item, cudaStream_t s);
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
+                           float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s);
+cudaError_t launch_quantize_e5m2(const __nv_bfloat16* x, long long n, uint8_t* q, float* amax_to_scale,
+                                 cudaStream_t s);
+cudaError_t launch_dequantize_e5m2(const uint8_t* q, const float* scale, long long n, __nv_bfloat16* y,
+                                   cudaStream_t s);
 cudaError_t launch_quantize_rows(const __nv_bfloat16* x, long long n, int cols, int rows_per_item,
                                  const float* amax, uint8_t* q, cudaStream_t s);
 cudaError_t launch_amax_items(const __nv_bfloat16* x, long long n, int cols, int rows_per_item, float* amax,

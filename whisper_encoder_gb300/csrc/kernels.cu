@@ -189,7 +189,7 @@ __device__ __forceinline__ void ln_load(const __nv_bfloat16* __restrict__ x, con
 // Persistent: warp w normalises the contiguous rows [w*R, (w+1)*R), loading row i+1 before it
 // reduces row i so that two rows of loads are in flight per warp.  amax (optional): per-item
 // absmax of the bf16 outputs, item = row / rows_per_item, one atomic per warp and item.
-template <int NV, int VEC, bool RES>
+template <int NV, int VEC, bool RES, bool RMS>
 __global__ void __launch_bounds__(LN_WARPS * 32)
     layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
                      const float* __restrict__ g, const float* __restrict__ bta, int rows, float eps,
@@ -228,12 +228,15 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
         }
       }
     }
-    float sm = 0.0f;
+    float mean = 0.0f;
+    if (!RMS) {   // RMSNorm skips the mean (and the beta shift)
+      float sm = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NV * VEC; ++i) sm += v[i];
+      for (int i = 0; i < NV * VEC; ++i) sm += v[i];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-    const float mean = sm * (1.0f / D);
+      for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      mean = sm * (1.0f / D);
+    }
     float q = 0.0f;
 #pragma unroll
     for (int i = 0; i < NV * VEC; ++i) {
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 #pragma unroll
       for (int j4 = 0; j4 < VEC / 4; ++j4) {
         const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + off) + j4);
-        const float4 b4 = __ldg(reinterpret_cast<const float4*>(bta + off) + j4);
+        const float4 b4 = RMS ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(bta + off) + j4);
         gg[4 * j4 + 0] = g4.x; gg[4 * j4 + 1] = g4.y; gg[4 * j4 + 2] = g4.z; gg[4 * j4 + 3] = g4.w;
         bb[4 * j4 + 0] = b4.x; bb[4 * j4 + 1] = b4.y; bb[4 * j4 + 2] = b4.z; bb[4 * j4 + 3] = b4.w;
       }
@@ -404,6 +407,37 @@ __global__ void amax_items_kernel(const __nv_bfloat16* __restrict__ x, long long
   (void)tid;
 }
 
+// E5M2 per-tensor cast: code = E5M2_rn_satfinite(x * 57344 / amax) (1 if amax == 0).
+__global__ void quantize_e5m2_kernel(const __nv_bfloat16* __restrict__ x, long long n, uint8_t* __restrict__ q,
+                                     const float* __restrict__ amax) {
+  const float a = *amax;
+  const float inv = a > 0.0f ? 57344.0f / a : 1.0f;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    uint16_t two;
+    const float v = __bfloat162float(x[i]) * inv;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(two) : "f"(0.0f), "f"(v));
+    q[i] = static_cast<uint8_t>(two & 0xFF);
+  }
+}
+
+__global__ void finalize_scale_e5m2_kernel(float* p) {
+  const float a = *p;
+  *p = a > 0.0f ? a / 57344.0f : 1.0f;
+}
+
+__global__ void dequantize_e5m2_kernel(const uint8_t* __restrict__ q, const float* __restrict__ scale, long long n,
+                                       __nv_bfloat16* __restrict__ y) {
+  const float s = *scale;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint16_t two = static_cast<uint16_t>(q[i]);
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(two));
+    y[i] = __float2bfloat16_rn(__half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFF))) * s);
+  }
+}
+
 __global__ void finalize_scale_kernel(float* p) {
   const float a = *p;
   *p = a > 0.0f ? a / 448.0f : 1.0f;
@@ -492,7 +526,7 @@ cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16*
   return cudaGetLastError();
 }
 
-template <int NV, int VEC>
+template <int NV, int VEC, bool RMS>
 static cudaError_t ln_launch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
                              int rows, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
                              int rows_per_item, cudaStream_t s) {
@@ -501,20 +535,21 @@ static cudaError_t ln_launch(const __nv_bfloat16* x, const __nv_bfloat16* res, c
   const long long cap = 2LL * sm_count();
   if (blocks > cap) blocks = cap;
   if (res)
-    layernorm_kernel<NV, VEC, true><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
+    layernorm_kernel<NV, VEC, true, RMS><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
         x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
   else
-    layernorm_kernel<NV, VEC, false><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
+    layernorm_kernel<NV, VEC, false, RMS><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
         x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
   return cudaGetLastError();
 }
 
-cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
-                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             int rows_per_item, cudaStream_t s) {
+template <bool RMS>
+static cudaError_t norm_dispatch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
+                                 int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
+                                 int rows_per_item, cudaStream_t s) {
 #define WB_LN_CASE(NV, VEC) \
   case NV * VEC * 32:       \
-    return ln_launch<NV, VEC>(x, res, g, b, rows, eps, y, total, amax, rows_per_item, s);
+    return ln_launch<NV, VEC, RMS>(x, res, g, b, rows, eps, y, total, amax, rows_per_item, s);
   switch (d) {
     WB_LN_CASE(1, 4)
     WB_LN_CASE(1, 8)
@@ -536,6 +571,17 @@ cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, c
       return cudaErrorInvalidValue;
   }
 #undef WB_LN_CASE
+}
+
+cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
+                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
+                             int rows_per_item, cudaStream_t s) {
+  return norm_dispatch<false>(x, res, g, b, rows, d, eps, y, total, amax, rows_per_item, s);
+}
+
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
+                           float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s) {
+  return norm_dispatch<true>(x, res, g, nullptr, rows, d, eps, y, total, nullptr, 0, s);
 }
 
 cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaStream_t s) {
@@ -564,6 +610,21 @@ cudaError_t launch_amax_items(const __nv_bfloat16* x, long long n, int cols, int
 
 cudaError_t launch_finalize_scale(float* amax_to_scale, cudaStream_t s) {
   finalize_scale_kernel<<<1, 1, 0, s>>>(amax_to_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_e5m2(const __nv_bfloat16* x, long long n, uint8_t* q, float* amax_to_scale,
+                                 cudaStream_t s) {
+  quantize_e5m2_kernel<<<grid_for(n, EW_THREADS), EW_THREADS, 0, s>>>(x, n, q, amax_to_scale);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  finalize_scale_e5m2_kernel<<<1, 1, 0, s>>>(amax_to_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize_e5m2(const uint8_t* q, const float* scale, long long n, __nv_bfloat16* y,
+                                   cudaStream_t s) {
+  dequantize_e5m2_kernel<<<grid_for(n, EW_THREADS), EW_THREADS, 0, s>>>(q, scale, n, y);
   return cudaGetLastError();
 }
 
