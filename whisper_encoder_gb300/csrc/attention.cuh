@@ -121,42 +121,49 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      auto pv = [&](int t, int jj) {
+      // Descriptors are built once: for these shared-memory addresses (below 256 KB) the
+      // descriptor of base + c is the descriptor of base plus c / 16, so every MMA only adds a
+      // compile-time offset.  The K/V stage index advances incrementally (no division).
+      const uint64_t q_desc0 = sw128_desc(smem_u32(smem + S::OFF_Q));
+      const uint64_t k_desc0 = sw128_desc(smem_u32(smem + S::OFF_K));
+      const uint64_t v_desc0 = sw128_desc(smem_u32(smem + S::OFF_V));
+      auto pv = [&](int t, int vst, bool first) {
         // P_t sits in the first 64 columns of S_t (two f16 per column): 8 columns per K16 step
-        const uint32_t sv = smem_u32(smem + S::OFF_V + (jj % ATT_STAGES) * S::V_BYTES);
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (S::V_BYTES >> 4));
         const uint32_t o_tm = tmem + 256 + t * 128;
+        const uint32_t p_tm = tmem + t * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k & 3) * 32;
-          mma_f16_tmem_a(o_tm, tmem + t * 128 + k * 8, sw128_desc(sv + (k >> 2) * S::VH_BYTES + off), IDESC_O,
-                         (jj | k) != 0);
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_f16_tmem_a(o_tm, p_tm + k * 8, vd + (((k >> 2) * S::VH_BYTES + (k & 3) * 32) >> 4), IDESC_O,
+                         (!first || k != 0) ? 1u : 0u);
         mma_commit(&o_done[t]);
       };
       bool ok = mbar_wait(q_full, 0, p.err, abort_flag, 12);
+      int st = 0, vst = 0;         // stage of K/V j, stage of V j-1
+      uint32_t kv_phase = 0;
       for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j % ATT_STAGES;
-        if (!mbar_wait(&kv_full[st], (j / ATT_STAGES) & 1, p.err, abort_flag, 13)) { ok = false; break; }
+        if (!mbar_wait(&kv_full[st], kv_phase, p.err, abort_flag, 13)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sk = smem_u32(smem + S::OFF_K + st * S::K_BYTES);
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>(st * (S::K_BYTES >> 4));
         for (int t = 0; t < ATT_TILES && ok; ++t) {
           if (j > 0) {
             if (!mbar_wait(&p_full[t], (j - 1) & 1, p.err, abort_flag, 14)) { ok = false; break; }
             tc_fence_after();
-            pv(t, j - 1);
+            pv(t, vst, j == 1);
           }
-          const uint32_t sq = smem_u32(smem + S::OFF_Q + t * S::Q_BYTES);
+          const uint64_t qd = q_desc0 + static_cast<uint64_t>(t * (S::Q_BYTES >> 4));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + t * 128, sw128_desc(sq + k * 32), sw128_desc(sk + k * 32), IDESC_S, k != 0);
+          for (int k = 0; k < 4; ++k) mma_bf16(tmem + t * 128, qd + 2 * k, kd + 2 * k, IDESC_S, k != 0);
           mma_commit(&s_full[t]);
         }
-        if (ok && j > 0) mma_commit(&kv_empty[(j - 1) % ATT_STAGES]);
+        if (ok && j > 0) mma_commit(&kv_empty[vst]);
+        vst = st;
+        if (++st == ATT_STAGES) { st = 0; kv_phase ^= 1u; }
       }
       for (int t = 0; t < ATT_TILES && ok; ++t) {
         if (!mbar_wait(&p_full[t], (nkv - 1) & 1, p.err, abort_flag, 15)) { ok = false; break; }
         tc_fence_after();
-        pv(t, nkv - 1);
+        pv(t, vst, nkv == 1);
       }
       mma_commit(mma_done);
       mbar_drain(mma_done, 0);
