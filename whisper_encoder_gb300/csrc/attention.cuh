@@ -3,19 +3,23 @@
 // The whisper-blaze showcase site, "The Solution" (flash_attn_hopper.cu card)
 // and "Impact" ("Attention without the quadratic write"): online softmax over
 // key tiles, scores never written to HBM.  Rebuilt on tcgen05:
-//   S_t = Q_t K_j^T        -> TMEM, fp32, one 128-column buffer per query tile
-//   P_t = 2^(S_t c - m_t)  -> f16, written back over S_t in TMEM (packed ex2: two
-//                             exponentials per MUFU op); the PV MMA reads its A operand from TMEM
-//   O_t += P_t [V_j | 1]   -> TMEM, fp32, 80 columns: 64 of output and 16 copies of the
-//                             row sum (a block of ones appended to V^T in shared memory)
-// A CTA owns two 128-query tiles of one (batch, head).  Warp 0 lane 0 loads
-// both Q tiles once and a ring of K / V^T tiles with TMA; warp 1 lane 0 issues
-// the MMAs, alternating between the tiles so that one tile's matrix products
-// run while the other tile's softmax runs; warps 2-17 split each query row of
-// the two tiles over two threads (64 score columns each).  The running max m_t is only moved
-// (and O rescaled in TMEM) when a new row maximum exceeds it by more than a
-// factor 2^8, which keeps every P entry below 256.  Keys past the sequence
-// end are masked to -inf; rows past it are not stored.
+//   S = Q K_j^T          -> TMEM, fp32, 128 columns
+//   P = 2^(S c - m)      -> f16 in TMEM, 64 columns (packed ex2: two exponentials per MUFU op);
+//                           the PV MMA reads its A operand from TMEM
+//   l += rowsum(P)       -> registers (packed f16 adds within a key tile, fp32 across tiles)
+//   O += P V_j           -> TMEM, fp32, 64 columns
+// A CTA owns one 128-query tile of one (batch, head) and 256 TMEM columns, so
+// two CTAs share an SM: one CTA's prologue (Q and first K/V loads) and epilogue
+// run under the other's main loop, and each has its own MMA issuer.  Warp 0
+// lane 0 loads Q once and rings of K and V^T tiles with TMA; warp 1 lane 0
+// issues the MMAs; warps 2-9 split each query row over two threads (64 score
+// columns each).  A softmax thread releases S as soon as it has loaded it into
+// registers, so QK of key tile j+1 runs while the softmax of key tile j is
+// still exponentiating; the softmax only waits for PV of key tile j-1 before
+// it overwrites P.  The running max m is only moved (and O rescaled in TMEM)
+// when a new row maximum exceeds it by more than a factor 2^8, which keeps
+// every P entry below 256.  Keys past the sequence end are masked to -inf;
+// rows past it are not stored.
 #pragma once
 #include "ptx.cuh"
 #include "types.h"
@@ -24,12 +28,12 @@ namespace wb {
 
 // q / k maps: 3-D (d, T, batch) views of the query and key rows (bf16), box (64, 128, 1)
 // vt map: 3-D (T, 64, batch*H) over V^T [batch*H][64][Tp] (f16), box (64, 64, 1)
-__global__ void __launch_bounds__(ATT_THREADS, 1)
+__global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
     attention_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap vt_map, const __grid_constant__ AttnParams p) {
   using S = AttnSmem;
   constexpr uint32_t IDESC_S = make_idesc(128, ATT_BKV, 1u);    // bf16 x bf16
-  constexpr uint32_t IDESC_O = make_idesc(128, ATT_NPV, 0u);    // f16 x f16
+  constexpr uint32_t IDESC_O = make_idesc(128, ATT_HD, 0u);     // f16 x f16
   constexpr float RESCALE_LOG2 = 8.0f;
 
   extern __shared__ uint8_t smem_raw[];
@@ -37,159 +41,163 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint8_t* smem = smem_raw + (base_u32 - smem_u32(smem_raw));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;                  // [STAGES]
-  uint64_t* kv_empty = kv_full + ATT_STAGES;     // [STAGES]
-  uint64_t* s_full = kv_empty + ATT_STAGES;      // [TILES]
-  uint64_t* p_full = s_full + ATT_TILES;         // [TILES]
-  uint64_t* o_done = p_full + ATT_TILES;         // [TILES]
-  uint64_t* xbar = o_done + ATT_TILES;           // [TILES][4]: row-max exchange between the two row halves
-  uint64_t* mma_done = xbar + ATT_TILES * 4;
+  uint64_t* k_full = q_full + 1;                 // [KSTAGES]
+  uint64_t* k_empty = k_full + ATT_KSTAGES;      // [KSTAGES]
+  uint64_t* v_full = k_empty + ATT_KSTAGES;      // [VSTAGES]
+  uint64_t* v_empty = v_full + ATT_VSTAGES;      // [VSTAGES]
+  uint64_t* s_full = v_empty + ATT_VSTAGES;      // QK done: S holds the scores
+  uint64_t* s_free = s_full + 1;                 // S loaded by all softmax warps
+  uint64_t* p_full = s_free + 1;                 // P written
+  uint64_t* pv_done = p_full + 1;                // PV done: P free, O stable
+  uint64_t* xbar = pv_done + 1;                  // [4]: row-max exchange between the two row halves
+  uint64_t* mma_done = xbar + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int n_qp = (p.T + ATT_TILES * ATT_BQ - 1) / (ATT_TILES * ATT_BQ);
-  const int qp = blockIdx.x % n_qp;
-  const int bh = blockIdx.x / n_qp;
+  const int n_qt = (p.T + ATT_BQ - 1) / ATT_BQ;
+  const int qt = blockIdx.x % n_qt;
+  const int bh = blockIdx.x / n_qt;
   const int b = bh / p.H, h = bh % p.H;
-  const int q0 = qp * ATT_TILES * ATT_BQ;
+  const int q0 = qt * ATT_BQ;
   const int nkv = (p.T + ATT_BKV - 1) / ATT_BKV;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < ATT_STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < ATT_KSTAGES; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    for (int t = 0; t < ATT_TILES; ++t) {
-      mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 4 * ATT_HALVES);
-      mbar_init(&o_done[t], 1);
-      for (int q = 0; q < 4; ++q) mbar_init(&xbar[t * 4 + q], ATT_HALVES);
+    for (int s = 0; s < ATT_VSTAGES; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4 * ATT_HALVES);
+    mbar_init(p_full, 4 * ATT_HALVES);
+    mbar_init(pv_done, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], ATT_HALVES);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp >= 2) {
-    // rows 64..79 of every V^T half tile hold f16 ones: their PV columns carry the row sums
-    constexpr int ONES_CHUNKS = (ATT_NPV - ATT_HD) * 128 / 16;     // 16-byte chunks per half tile
-    const int n16 = ATT_STAGES * 2 * ONES_CHUNKS;
-    for (int i = threadIdx.x - 64; i < n16; i += ATT_THREADS - 64) {
-      const int half = i / ONES_CHUNKS, within = i % ONES_CHUNKS;
-      uint8_t* dst = smem + S::OFF_V + half * S::VH_BYTES + ATT_HD * 128 + within * 16;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-    }
-    fence_proxy_async_smem();
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tmem_alloc(tmem_slot, ATT_TM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S_t at 128 t, O_t at 256 + 128 t (80 columns each).
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&k_map);
       tma_prefetch_desc(&vt_map);
-      mbar_arrive_expect_tx(q_full, ATT_TILES * S::Q_BYTES);
-      for (int t = 0; t < ATT_TILES; ++t)
-        tma_load_3d(smem + S::OFF_Q + t * S::Q_BYTES, &q_map, q_full, h * ATT_HD, q0 + t * ATT_BQ, b);
-      uint32_t issued = 0, last_par = 0;
-      bool ok = true;
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int st = j % ATT_STAGES;
-        const uint32_t ph = (j / ATT_STAGES) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1u, p.err, abort_flag, 11)) { ok = false; break; }
-        mbar_arrive_expect_tx(&kv_full[st], S::K_BYTES + 2 * ATT_HD * 128);
-        const int kv0 = j * ATT_BKV;
-        tma_load_3d(smem + S::OFF_K + st * S::K_BYTES, &k_map, &kv_full[st], h * ATT_HD, kv0, b);
+      mbar_arrive_expect_tx(q_full, S::Q_BYTES);
+      tma_load_3d(smem + S::OFF_Q, &q_map, q_full, h * ATT_HD, q0, b);
+      // Load order K_0, then (K_{i+1}, V_i): the MMA warp consumes K one key tile ahead of V.
+      uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
+      auto load_k = [&](int jj) -> bool {
+        const int st = jj % ATT_KSTAGES;
+        const uint32_t ph = (jj / ATT_KSTAGES) & 1;
+        if (!mbar_wait(&k_empty[st], ph ^ 1u, p.err, abort_flag, 11)) return false;
+        mbar_arrive_expect_tx(&k_full[st], S::K_BYTES);
+        tma_load_3d(smem + S::OFF_K + st * S::K_BYTES, &k_map, &k_full[st], h * ATT_HD, jj * ATT_BKV, b);
+        k_issued |= 1u << st;
+        k_par = (k_par & ~(1u << st)) | (ph << st);
+        return true;
+      };
+      auto load_v = [&](int jj) -> bool {
+        const int st = jj % ATT_VSTAGES;
+        const uint32_t ph = (jj / ATT_VSTAGES) & 1;
+        if (!mbar_wait(&v_empty[st], ph ^ 1u, p.err, abort_flag, 10)) return false;
+        mbar_arrive_expect_tx(&v_full[st], S::V_BYTES);
         uint8_t* vdst = smem + S::OFF_V + st * S::V_BYTES;
-        tma_load_3d(vdst, &vt_map, &kv_full[st], kv0, 0, bh);
-        tma_load_3d(vdst + S::VH_BYTES, &vt_map, &kv_full[st], kv0 + 64, 0, bh);
-        issued |= 1u << st;
-        last_par = (last_par & ~(1u << st)) | (ph << st);
+        tma_load_3d(vdst, &vt_map, &v_full[st], jj * ATT_BKV, 0, bh);
+        tma_load_3d(vdst + S::VH_BYTES, &vt_map, &v_full[st], jj * ATT_BKV + 64, 0, bh);
+        v_issued |= 1u << st;
+        v_par = (v_par & ~(1u << st)) | (ph << st);
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int i = 0; i < nkv && ok; ++i) {
+        if (i + 1 < nkv) ok = load_k(i + 1);
+        ok = ok && load_v(i);
       }
       if (!ok) {
+        // copies already issued still land in shared memory: wait for them before the CTA exits
         mbar_drain(q_full, 0);
-        for (int s = 0; s < ATT_STAGES; ++s)
-          if (issued & (1u << s)) mbar_drain(&kv_full[s], (last_par >> s) & 1u);
+        for (int s = 0; s < ATT_KSTAGES; ++s)
+          if (k_issued & (1u << s)) mbar_drain(&k_full[s], (k_par >> s) & 1u);
+        for (int s = 0; s < ATT_VSTAGES; ++s)
+          if (v_issued & (1u << s)) mbar_drain(&v_full[s], (v_par >> s) & 1u);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // Descriptors are built once: for these shared-memory addresses (below 256 KB) the
-      // descriptor of base + c is the descriptor of base plus c / 16, so every MMA only adds a
-      // compile-time offset.  The K/V stage index advances incrementally (no division).
-      const uint64_t q_desc0 = sw128_desc(smem_u32(smem + S::OFF_Q));
+      // For these shared-memory addresses (below 256 KB) the descriptor of base + c is the
+      // descriptor of base plus c / 16, so every MMA only adds an offset.
+      const uint64_t q_desc = sw128_desc(smem_u32(smem + S::OFF_Q));
       const uint64_t k_desc0 = sw128_desc(smem_u32(smem + S::OFF_K));
       const uint64_t v_desc0 = sw128_desc(smem_u32(smem + S::OFF_V));
-      auto pv = [&](int t, int vst, bool first) {
-        // P_t sits in the first 64 columns of S_t (two f16 per column): 8 columns per K16 step
-        const uint64_t vd = v_desc0 + static_cast<uint64_t>(vst * (S::V_BYTES >> 4));
-        const uint32_t o_tm = tmem + 256 + t * 128;
-        const uint32_t p_tm = tmem + t * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_f16_tmem_a(o_tm, p_tm + k * 8, vd + (((k >> 2) * S::VH_BYTES + (k & 3) * 32) >> 4), IDESC_O,
-                         (!first || k != 0) ? 1u : 0u);
-        mma_commit(&o_done[t]);
-      };
-      bool ok = mbar_wait(q_full, 0, p.err, abort_flag, 12);
-      int st = 0, vst = 0;         // stage of K/V j, stage of V j-1
-      uint32_t kv_phase = 0;
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (!mbar_wait(&kv_full[st], kv_phase, p.err, abort_flag, 13)) { ok = false; break; }
+      auto qk = [&](int jj) -> bool {
+        // S = Q K_jj^T once K_jj has landed and the softmax has loaded S of key tile jj - 1
+        const int st = jj % ATT_KSTAGES;
+        if (!mbar_wait(&k_full[st], (jj / ATT_KSTAGES) & 1, p.err, abort_flag, 13)) return false;
+        if (jj > 0 && !mbar_wait(s_free, (jj - 1) & 1, p.err, abort_flag, 20)) return false;
         tc_fence_after();
         const uint64_t kd = k_desc0 + static_cast<uint64_t>(st * (S::K_BYTES >> 4));
-        for (int t = 0; t < ATT_TILES && ok; ++t) {
-          if (j > 0) {
-            if (!mbar_wait(&p_full[t], (j - 1) & 1, p.err, abort_flag, 14)) { ok = false; break; }
-            tc_fence_after();
-            pv(t, vst, j == 1);
-          }
-          const uint64_t qd = q_desc0 + static_cast<uint64_t>(t * (S::Q_BYTES >> 4));
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_bf16(tmem + t * 128, qd + 2 * k, kd + 2 * k, IDESC_S, k != 0);
-          mma_commit(&s_full[t]);
-        }
-        if (ok && j > 0) mma_commit(&kv_empty[vst]);
-        vst = st;
-        if (++st == ATT_STAGES) { st = 0; kv_phase ^= 1u; }
-      }
-      for (int t = 0; t < ATT_TILES && ok; ++t) {
-        if (!mbar_wait(&p_full[t], (nkv - 1) & 1, p.err, abort_flag, 15)) { ok = false; break; }
+        for (int k = 0; k < 4; ++k) mma_bf16(tmem + ATT_TM_S, q_desc + 2 * k, kd + 2 * k, IDESC_S, k != 0);
+        mma_commit(s_full);
+        mma_commit(&k_empty[st]);
+        return true;
+      };
+      auto pv = [&](int jj) -> bool {
+        // O += P V_jj; P holds 128 keys as 64 packed f16 columns: 8 columns per K16 step
+        const int st = jj % ATT_VSTAGES;
+        if (!mbar_wait(&v_full[st], (jj / ATT_VSTAGES) & 1, p.err, abort_flag, 21)) return false;
+        if (!mbar_wait(p_full, jj & 1, p.err, abort_flag, 14)) return false;
         tc_fence_after();
-        pv(t, vst, nkv == 1);
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(st * (S::V_BYTES >> 4));
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_f16_tmem_a(tmem + ATT_TM_O, tmem + ATT_TM_P + k * 8,
+                         vd + (((k >> 2) * S::VH_BYTES + (k & 3) * 32) >> 4), IDESC_O,
+                         (jj > 0 || k != 0) ? 1u : 0u);
+        mma_commit(pv_done);
+        mma_commit(&v_empty[st]);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag, 12) && qk(0);
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (j + 1 < nkv) ok = qk(j + 1);
+        ok = ok && pv(j);
       }
       mma_commit(mma_done);
       mbar_drain(mma_done, 0);
     }
   } else {
     // --------------------------- softmax / output --------------------------
-    // 16 warps: tile t = sw / 8, row half hf = (sw / 4) % 2 (score columns 64 hf .. 64 hf + 63),
-    // TMEM lane quarter = warp % 4.  The two threads holding the halves of one row exchange
-    // their half-row maxima through shared memory (one mbarrier per tile and lane quarter).
-    const int sw = warp - 2;
-    const int t = sw >> 3;
-    const int hf = (sw >> 2) & 1;
+    // 8 warps: row half hf = (warp - 2) / 4 (score columns 64 hf .. 64 hf + 63), TMEM lane
+    // quarter = warp % 4.  The two threads holding the halves of one row exchange their
+    // half-row maxima through shared memory (one mbarrier per lane quarter).
+    const int hf = ((warp - 2) >> 2) & 1;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;             // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + t * 128 + hf * 64;
-    const uint32_t o_tm = tmem + lane_off + 256 + t * 128;
-    const uint32_t p_tm = tmem + lane_off + t * 128 + hf * 32;   // this half's 32 packed P columns
+    const uint32_t s_tm = tmem + lane_off + ATT_TM_S + hf * 64;
+    const uint32_t o_tm = tmem + lane_off + ATT_TM_O + hf * 32;   // this half's 32 output columns
+    const uint32_t p_tm = tmem + lane_off + ATT_TM_P + hf * 32;   // this half's 32 packed P columns
     float* xmax = reinterpret_cast<float*>(smem + S::OFF_XMAX);
-    uint64_t* xb = &xbar[t * 4 + quarter];
+    uint64_t* xb = &xbar[quarter];
     const float c = p.scale_log2;
     float m_use = -INFINITY;
+    float l_run = 0.0f;                            // this half's share of the row sum, scaled like O
     bool ok = true;
 
     for (int j = 0; j < nkv && ok; ++j) {
-      if (!mbar_wait(&s_full[t], j & 1, p.err, abort_flag, 16)) { ok = false; break; }
+      if (!mbar_wait(s_full, j & 1, p.err, abort_flag, 16)) { ok = false; break; }
       tc_fence_after();
       float s[64];
       {
@@ -202,6 +210,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
       }
       tmem_ld_wait();
+      tc_fence_before();           // S is in registers: QK of the next key tile may overwrite it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
       const int valid = p.T - j * ATT_BKV - hf * 64;      // columns of this half inside the sequence
       if (valid < 64) {
 #pragma unroll
@@ -216,13 +227,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
       }
       const float own = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-      float* xm = xmax + ((j & 1) * ATT_TILES + t) * ATT_HALVES * ATT_BQ;
+      float* xm = xmax + (j & 1) * ATT_HALVES * ATT_BQ;
       xm[hf * ATT_BQ + r] = own;
-      tc_fence_before();           // this half's TMEM loads of S precede the partner's P stores
       __syncwarp();
       if (lane == 0) mbar_arrive(xb);
       if (!mbar_wait(xb, j & 1, p.err, abort_flag, 19)) { ok = false; break; }
-      tc_fence_after();
       const float mx = fmaxf(own, xm[(1 - hf) * ATT_BQ + r]);
       const float m_cand = mx * c;
       float alpha = 1.0f;
@@ -233,51 +242,62 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         alpha = ex2_approx(m_use - m_cand);
         m_use = m_cand;
         rescale = true;
-      }
-      if (j > 0) {
-        // PV of the previous step is complete: P may be overwritten and O is stable until PV(j) is issued
-        if (!mbar_wait(&o_done[t], (j - 1) & 1, p.err, abort_flag, 17)) { ok = false; break; }
-        tc_fence_after();
+        l_run *= alpha;
       }
       const float mb = -m_use;
       uint32_t pw[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) pw[i] = ex2_f16x2(pack_f16(fmaf(s[2 * i], c, mb), fmaf(s[2 * i + 1], c, mb)));
-      // Half 1's P columns (32..63) overlay half 0's scores; half 0 finished reading them before
-      // it arrived at the row-max exchange, which half 1 has passed.
+      {
+        // row sum of the 64 f16 entries: pairwise packed adds (partial sums stay below 2^13), then fp32
+        uint32_t a[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = hadd2_u32(pw[2 * i], pw[2 * i + 1]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+          for (int i = 0; i < w; ++i) a[i] = hadd2_u32(a[i], a[i + w]);
+        }
+        l_run += f16x2_sum_f32(a[0]);
+      }
+      // PV of key tile j-1 is done: P may be overwritten and O is stable until PV of tile j is issued
+      if (j > 0) {
+        if (!mbar_wait(pv_done, (j - 1) & 1, p.err, abort_flag, 17)) { ok = false; break; }
+        tc_fence_after();
+      }
       tmem_st32u(p_tm, pw);
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // half 0 rescales O columns 0..31 and the row sums 64..79, half 1 columns 32..63
+        // each half rescales its 32 of the 64 O columns
         float v[32];
-        tmem_ld32(o_tm + hf * 32, v);
+        tmem_ld32(o_tm, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(o_tm + hf * 32, v);
-        if (hf == 0) {
-          float w[16];
-          tmem_ld16(o_tm + 64, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] *= alpha;
-          tmem_st16(o_tm + 64, w);
-        }
-        tmem_st_wait();
+        tmem_st32(o_tm, v);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[t]);
+      if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && mbar_wait(&o_done[t], (nkv - 1) & 1, p.err, abort_flag, 18)) {
+    if (ok) {
+      // full row sum: the two halves swap their shares through the max-exchange buffer of parity
+      // nkv (both halves have finished reading it at step nkv - 2)
+      float* xl = xmax + (nkv & 1) * ATT_HALVES * ATT_BQ;
+      xl[hf * ATT_BQ + r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xb);
+      ok = mbar_wait(xb, nkv & 1, p.err, abort_flag, 22);
+      if (ok) l_run += xl[(1 - hf) * ATT_BQ + r];
+    }
+    if (ok && mbar_wait(pv_done, (nkv - 1) & 1, p.err, abort_flag, 18)) {
       tc_fence_after();
-      float o[32], w[16];
-      tmem_ld32(o_tm + hf * 32, o);
-      tmem_ld16(o_tm + 64, w);
+      float o[32];
+      tmem_ld32(o_tm, o);
       tmem_ld_wait();
-      const int q = q0 + t * ATT_BQ + r;
+      const int q = q0 + r;
       if (q < p.T) {
-        const float inv = 1.0f / w[0];
+        const float inv = 1.0f / l_run;
         uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.T + q) * p.d + h * ATT_HD + hf * 32);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -293,7 +313,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, ATT_TM_COLS);
 }
 
 }  // namespace wb

@@ -298,6 +298,21 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
   return r;
 }
 
+// Packed f16x2 add (round to nearest).
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Sum of the two halves of a packed f16x2, in fp32.
+__device__ __forceinline__ float f16x2_sum_f32(uint32_t a) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(a));
+  return lo + hi;
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

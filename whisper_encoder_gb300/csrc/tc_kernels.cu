@@ -94,8 +94,8 @@ cudaError_t launch_attention(const CUtensorMap& q, const CUtensorMap& k, const C
   static uint64_t attr_done = 0;
   cudaError_t e = ensure_smem_attr(attention_kernel, smem, &attr_done);
   if (e != cudaSuccess) return e;
-  const int n_qp = (p.T + ATT_TILES * ATT_BQ - 1) / (ATT_TILES * ATT_BQ);
-  const long long grid = static_cast<long long>(p.batch) * p.H * n_qp;
+  const int n_qt = (p.T + ATT_BQ - 1) / ATT_BQ;
+  const long long grid = static_cast<long long>(p.batch) * p.H * n_qt;
   if (grid < 1) return cudaSuccess;
   attention_kernel<<<static_cast<unsigned>(grid), ATT_THREADS, smem, s>>>(q, k, vt, p);
   return cudaGetLastError();

@@ -61,27 +61,31 @@ struct GemmParams {
   uint32_t* err;
 };
 
-constexpr int ATT_BQ = 128;           // queries per tile; a CTA owns two tiles
-constexpr int ATT_TILES = 2;
+constexpr int ATT_BQ = 128;           // queries per CTA
 constexpr int ATT_BKV = 128;          // keys per step
 constexpr int ATT_HD = 64;            // head dim
-constexpr int ATT_NPV = 80;           // PV MMA width: 64 value columns + 16 columns of ones (row sums)
-constexpr int ATT_STAGES = 5;
+constexpr int ATT_KSTAGES = 3;        // K tiles in flight
+constexpr int ATT_VSTAGES = 2;        // V^T tiles in flight
 constexpr int ATT_HALVES = 2;         // each score row is split over two softmax threads (64 columns each)
-constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_TILES * ATT_HALVES;   // producer + MMA + softmax warps
+constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_HALVES;   // producer + MMA + 8 softmax warps
+constexpr int ATT_CTAS_PER_SM = 2;
+// TMEM columns of one CTA (two CTAs share the 512 of an SM): S (128 fp32), O (64 fp32),
+// P (128 keys as 64 packed f16 columns).
+constexpr uint32_t ATT_TM_S = 0, ATT_TM_O = 128, ATT_TM_P = 192, ATT_TM_COLS = 256;
 
 struct AttnSmem {
   static constexpr int Q_BYTES = ATT_BQ * 128;              // [128 q][64 e] bf16
   static constexpr int K_BYTES = ATT_BKV * 128;             // [128 kv][64 e] bf16
-  static constexpr int VH_BYTES = ATT_NPV * 128;            // one V^T half: [64 e][64 kv] f16 + 16 rows of ones
+  static constexpr int VH_BYTES = ATT_HD * 128;             // one V^T half: [64 e][64 kv] f16
   static constexpr int V_BYTES = 2 * VH_BYTES;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + ATT_TILES * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + ATT_STAGES * K_BYTES;
-  static constexpr int OFF_XMAX = OFF_V + ATT_STAGES * V_BYTES;             // [2 parity][tile][half][128] f32
-  static constexpr int OFF_BAR = OFF_XMAX + 2 * ATT_TILES * ATT_HALVES * ATT_BQ * 4;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + ATT_KSTAGES * K_BYTES;
+  static constexpr int OFF_XMAX = OFF_V + ATT_VSTAGES * V_BYTES;            // [2 parity][half][128] f32
+  static constexpr int OFF_BAR = OFF_XMAX + 2 * ATT_HALVES * ATT_BQ * 4;
   static constexpr int TOTAL = 1024 + OFF_BAR + 256;
 };
+static_assert(2 * AttnSmem::TOTAL <= 227 * 1024, "two attention CTAs must fit one SM");
 
 struct AttnParams {
   int T;            // sequence length (1500)
