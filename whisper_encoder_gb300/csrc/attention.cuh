@@ -12,8 +12,8 @@
 // two CTAs share an SM: one CTA's prologue (Q and first K/V loads) and epilogue
 // run under the other's main loop, and each has its own MMA issuer.  Warp 0
 // lane 0 loads Q once and rings of K and V^T tiles with TMA; warp 1 lane 0
-// issues the MMAs; warps 2-9 split each query row over two threads (64 score
-// columns each).  A softmax thread releases S as soon as it has loaded it into
+// issues the MMAs; warps 2-9 run the softmax, each row held by four threads of
+// one warp (32 score columns each).  A softmax thread releases S as soon as it has loaded it into
 // registers, so QK of key tile j+1 runs while the softmax of key tile j is
 // still exponentiating; the softmax only waits for PV of key tile j-1 before
 // it overwrites P.  The running max m is only moved (and O rescaled in TMEM)
@@ -49,8 +49,7 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
   uint64_t* s_free = s_full + 1;                 // S loaded by all softmax warps
   uint64_t* p_full = s_free + 1;                 // P written
   uint64_t* pv_done = p_full + 1;                // PV done: P free, O stable
-  uint64_t* xbar = pv_done + 1;                  // [4]: row-max exchange between the two row halves
-  uint64_t* mma_done = xbar + 4;
+  uint64_t* mma_done = pv_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -74,10 +73,9 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
       mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 4 * ATT_HALVES);
-    mbar_init(p_full, 4 * ATT_HALVES);
+    mbar_init(s_free, ATT_SOFTMAX_WARPS);
+    mbar_init(p_full, ATT_SOFTMAX_WARPS);
     mbar_init(pv_done, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], ATT_HALVES);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -179,133 +177,164 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
     }
   } else {
     // --------------------------- softmax / output --------------------------
-    // 8 warps: row half hf = (warp - 2) / 4 (score columns 64 hf .. 64 hf + 63), TMEM lane
-    // quarter = warp % 4.  The two threads holding the halves of one row exchange their
-    // half-row maxima through shared memory (one mbarrier per lane quarter).
-    const int hf = ((warp - 2) >> 2) & 1;
+    // 8 warps; warp w owns the 16 TMEM lanes (query rows) 32 (w % 4) + 16 sub .. + 15, sub = (w - 2) / 4.
+    // With the 16-lane TMEM shapes thread t holds rows ra = t/4 and ra + 8 of that block and, of each,
+    // the score columns 8k + 2 (t % 4) and + 1 (k = 0..15): 32 of the row's 128 scores.  The four
+    // threads that share a row combine row maxima with two shuffles and keep partial row sums.  A
+    // thread's pair of adjacent scores becomes one packed f16 P column, 4k + t % 4, which is where the
+    // 16x128b store shape puts it.  Waits are made warp-uniform so that a timeout leaves no lane behind.
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;             // query row inside the tile
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + ATT_TM_S + hf * 64;
-    const uint32_t o_tm = tmem + lane_off + ATT_TM_O + hf * 32;   // this half's 32 output columns
-    const uint32_t p_tm = tmem + lane_off + ATT_TM_P + hf * 32;   // this half's 32 packed P columns
-    float* xmax = reinterpret_cast<float*>(smem + S::OFF_XMAX);
-    uint64_t* xb = &xbar[quarter];
+    const int sub = ((warp - 2) >> 2) & 1;
+    const int lane_base = quarter * 32 + sub * 16;
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    const uint32_t s_tm = tmem + lane_off + ATT_TM_S;
+    const uint32_t o_tm = tmem + lane_off + ATT_TM_O;
+    const uint32_t p_tm = tmem + lane_off + ATT_TM_P;
+    const int ra = lane_base + (lane >> 2);        // first of this thread's two rows inside the tile
+    const int cq = 2 * (lane & 3);                 // this thread's column offset in every 8-column group
     const float c = p.scale_log2;
-    float m_use = -INFINITY;
-    float l_run = 0.0f;                            // this half's share of the row sum, scaled like O
+    float m_a = -INFINITY, m_b = -INFINITY;        // running maxima (log2 units) of rows ra and ra + 8
+    float l_a = 0.0f, l_b = 0.0f;                  // this thread's share of the two row sums, scaled like O
     bool ok = true;
 
     for (int j = 0; j < nkv && ok; ++j) {
-      if (!mbar_wait(s_full, j & 1, p.err, abort_flag, 16)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, p.err, abort_flag, 16))) { ok = false; break; }
       tc_fence_after();
+      // s[4k], s[4k+1]: row ra, columns 8k + cq, + 1; s[4k+2], s[4k+3]: row ra + 8, same columns
       float s[64];
       {
-        float v[32];
-        tmem_ld32(s_tm, v);
+        uint32_t v[32];
+        tmem_ld_16x256b_x8(s_tm, v);               // columns 0..63
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = v[i];
-        tmem_ld32(s_tm + 32, v);
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(v[i]);
+        tmem_ld_16x256b_x8(s_tm + 64, v);          // columns 64..127
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
+        for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(v[i]);
       }
       tmem_ld_wait();
       tc_fence_before();           // S is in registers: QK of the next key tile may overwrite it
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      const int valid = p.T - j * ATT_BKV - hf * 64;      // columns of this half inside the sequence
-      if (valid < 64) {
+      const int valid = p.T - j * ATT_BKV;         // key columns of this tile inside the sequence
+      if (valid < ATT_BKV) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = (i < valid) ? s[i] : -INFINITY;
+        for (int kk = 0; kk < 16; ++kk) {
+          const int col = 8 * kk + cq;
+          if (col >= valid) s[4 * kk] = s[4 * kk + 2] = -INFINITY;
+          if (col + 1 >= valid) s[4 * kk + 1] = s[4 * kk + 3] = -INFINITY;
+        }
       }
-      float m4[4];
+      float xa0 = fmaxf(s[0], s[1]), xa1 = fmaxf(s[4], s[5]);
+      float xb0 = fmaxf(s[2], s[3]), xb1 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) m4[k] = fmaxf(s[2 * k], s[2 * k + 1]);       // s[0..7]
-#pragma unroll
-      for (int i = 8; i < 64; i += 8) {                                          // s[8..63], 8 per step
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m4[k] = fmax3(m4[k], s[i + 2 * k], s[i + 2 * k + 1]);
+      for (int kk = 2; kk < 16; kk += 2) {
+        xa0 = fmax3(xa0, s[4 * kk], s[4 * kk + 1]);
+        xa1 = fmax3(xa1, s[4 * kk + 4], s[4 * kk + 5]);
+        xb0 = fmax3(xb0, s[4 * kk + 2], s[4 * kk + 3]);
+        xb1 = fmax3(xb1, s[4 * kk + 6], s[4 * kk + 7]);
       }
-      const float own = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-      float* xm = xmax + (j & 1) * ATT_HALVES * ATT_BQ;
-      xm[hf * ATT_BQ + r] = own;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xb);
-      if (!mbar_wait(xb, j & 1, p.err, abort_flag, 19)) { ok = false; break; }
-      const float mx = fmaxf(own, xm[(1 - hf) * ATT_BQ + r]);
-      const float m_cand = mx * c;
-      float alpha = 1.0f;
+      float xa = fmaxf(xa0, xa1), xb = fmaxf(xb0, xb1);
+      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
+      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
+      const float ca = xa * c, cb = xb * c;
+      float alpha_a = 1.0f, alpha_b = 1.0f;
       bool rescale = false;
       if (j == 0) {
-        m_use = m_cand;
-      } else if (m_cand > m_use + RESCALE_LOG2) {
-        alpha = ex2_approx(m_use - m_cand);
-        m_use = m_cand;
-        rescale = true;
-        l_run *= alpha;
+        m_a = ca;
+        m_b = cb;
+      } else {
+        if (ca > m_a + RESCALE_LOG2) {
+          alpha_a = ex2_approx(m_a - ca);
+          m_a = ca;
+          l_a *= alpha_a;
+          rescale = true;
+        }
+        if (cb > m_b + RESCALE_LOG2) {
+          alpha_b = ex2_approx(m_b - cb);
+          m_b = cb;
+          l_b *= alpha_b;
+          rescale = true;
+        }
       }
-      const float mb = -m_use;
+      // pw[2k]: row ra, P column 4k + t % 4 (keys 8k + cq, + 1); pw[2k+1]: row ra + 8, same column
+      const uint64_t c2 = f32x2_pack(c, c), na2 = f32x2_pack(-m_a, -m_a), nb2 = f32x2_pack(-m_b, -m_b);
       uint32_t pw[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) pw[i] = ex2_f16x2(pack_f16(fmaf(s[2 * i], c, mb), fmaf(s[2 * i + 1], c, mb)));
+      for (int kk = 0; kk < 16; ++kk) {
+        float x0, x1, x2, x3;
+        fma_f32x2(x0, x1, s[4 * kk], s[4 * kk + 1], c2, na2);
+        fma_f32x2(x2, x3, s[4 * kk + 2], s[4 * kk + 3], c2, nb2);
+        pw[2 * kk] = ex2_f16x2(pack_f16(x0, x1));
+        pw[2 * kk + 1] = ex2_f16x2(pack_f16(x2, x3));
+      }
       {
-        // row sum of the 64 f16 entries: pairwise packed adds (partial sums stay below 2^13), then fp32
-        uint32_t a[16];
+        // partial row sums of the 32 f16 entries per row: pairwise packed adds (partial sums stay
+        // below 2^12), then fp32
+        uint32_t a[8], bq[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) a[i] = hadd2_u32(pw[2 * i], pw[2 * i + 1]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-          for (int i = 0; i < w; ++i) a[i] = hadd2_u32(a[i], a[i + w]);
+        for (int i = 0; i < 8; ++i) {
+          a[i] = hadd2_u32(pw[4 * i], pw[4 * i + 2]);
+          bq[i] = hadd2_u32(pw[4 * i + 1], pw[4 * i + 3]);
         }
-        l_run += f16x2_sum_f32(a[0]);
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1) {
+#pragma unroll
+          for (int i = 0; i < w; ++i) {
+            a[i] = hadd2_u32(a[i], a[i + w]);
+            bq[i] = hadd2_u32(bq[i], bq[i + w]);
+          }
+        }
+        l_a += f16x2_sum_f32(a[0]);
+        l_b += f16x2_sum_f32(bq[0]);
       }
       // PV of key tile j-1 is done: P may be overwritten and O is stable until PV of tile j is issued
       if (j > 0) {
-        if (!mbar_wait(pv_done, (j - 1) & 1, p.err, abort_flag, 17)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, p.err, abort_flag, 17))) { ok = false; break; }
         tc_fence_after();
       }
-      tmem_st32u(p_tm, pw);
+      tmem_st_16x128b_x16(p_tm, pw);
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // each half rescales its 32 of the 64 O columns
-        float v[32];
-        tmem_ld32(o_tm, v);
+        uint32_t v[32];
+        tmem_ld_16x256b_x8(o_tm, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-        tmem_st32(o_tm, v);
+        for (int kk = 0; kk < 8; ++kk) {
+          v[4 * kk] = __float_as_uint(__uint_as_float(v[4 * kk]) * alpha_a);
+          v[4 * kk + 1] = __float_as_uint(__uint_as_float(v[4 * kk + 1]) * alpha_a);
+          v[4 * kk + 2] = __float_as_uint(__uint_as_float(v[4 * kk + 2]) * alpha_b);
+          v[4 * kk + 3] = __float_as_uint(__uint_as_float(v[4 * kk + 3]) * alpha_b);
+        }
+        tmem_st_16x256b_x8(o_tm, v);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok) {
-      // full row sum: the two halves swap their shares through the max-exchange buffer of parity
-      // nkv (both halves have finished reading it at step nkv - 2)
-      float* xl = xmax + (nkv & 1) * ATT_HALVES * ATT_BQ;
-      xl[hf * ATT_BQ + r] = l_run;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xb);
-      ok = mbar_wait(xb, nkv & 1, p.err, abort_flag, 22);
-      if (ok) l_run += xl[(1 - hf) * ATT_BQ + r];
-    }
-    if (ok && mbar_wait(pv_done, (nkv - 1) & 1, p.err, abort_flag, 18)) {
+    // full row sums from the four threads of each row
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    if (ok && __all_sync(0xffffffffu, mbar_wait(pv_done, (nkv - 1) & 1, p.err, abort_flag, 18))) {
       tc_fence_after();
-      float o[32];
-      tmem_ld32(o_tm, o);
+      uint32_t v[32];                              // [4k..4k+3]: rows ra / ra + 8, columns 8k + cq, + 1
+      tmem_ld_16x256b_x8(o_tm, v);
       tmem_ld_wait();
-      const int q = q0 + r;
-      if (q < p.T) {
-        const float inv = 1.0f / l_run;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<long long>(b) * p.T + q) * p.d + h * ATT_HD + hf * 32);
+      const float ia = 1.0f / l_a, ib = 1.0f / l_b;
+      const int qa = q0 + ra, qb = qa + 8;
+      __nv_bfloat16* oa = p.out + (static_cast<long long>(b) * p.T + qa) * p.d + h * ATT_HD + cq;
+      __nv_bfloat16* ob = oa + 8LL * p.d;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          dst[k] = make_uint4(pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv),
-                              pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
-                              pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
-                              pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
-        }
+      for (int kk = 0; kk < 8; ++kk) {
+        if (qa < p.T)
+          *reinterpret_cast<uint32_t*>(oa + 8 * kk) =
+              pack_bf16(__uint_as_float(v[4 * kk]) * ia, __uint_as_float(v[4 * kk + 1]) * ia);
+        if (qb < p.T)
+          *reinterpret_cast<uint32_t*>(ob + 8 * kk) =
+              pack_bf16(__uint_as_float(v[4 * kk + 2]) * ib, __uint_as_float(v[4 * kk + 3]) * ib);
       }
     }
   }

@@ -66,8 +66,8 @@ constexpr int ATT_BKV = 128;          // keys per step
 constexpr int ATT_HD = 64;            // head dim
 constexpr int ATT_KSTAGES = 3;        // K tiles in flight
 constexpr int ATT_VSTAGES = 2;        // V^T tiles in flight
-constexpr int ATT_HALVES = 2;         // each score row is split over two softmax threads (64 columns each)
-constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_HALVES;   // producer + MMA + 8 softmax warps
+constexpr int ATT_SOFTMAX_WARPS = 8;  // two per TMEM lane quarter, 16 query rows each
+constexpr int ATT_THREADS = 64 + 32 * ATT_SOFTMAX_WARPS;   // producer + MMA + softmax warps
 constexpr int ATT_CTAS_PER_SM = 2;
 // TMEM columns of one CTA (two CTAs share the 512 of an SM): S (128 fp32), O (64 fp32),
 // P (128 keys as 64 packed f16 columns).
@@ -81,8 +81,7 @@ struct AttnSmem {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + ATT_KSTAGES * K_BYTES;
-  static constexpr int OFF_XMAX = OFF_V + ATT_VSTAGES * V_BYTES;            // [2 parity][half][128] f32
-  static constexpr int OFF_BAR = OFF_XMAX + 2 * ATT_HALVES * ATT_BQ * 4;
+  static constexpr int OFF_BAR = OFF_V + ATT_VSTAGES * V_BYTES;
   static constexpr int TOTAL = 1024 + OFF_BAR + 256;
 };
 static_assert(2 * AttnSmem::TOTAL <= 227 * 1024, "two attention CTAs must fit one SM");
