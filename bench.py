@@ -230,7 +230,8 @@ def run_case(args) -> None:
         n, k = {"fc1": (F, d), "fc2": (d, F), "qkv": (3 * d, d), "out": (d, d)}[args.case]
         a, w = rnd(M, k), rnd(n, k, scale=0.02)
         bias = torch.zeros(n, device="cuda")
-        fn = lambda: wb.linear(a, w, bias=bias, gelu=args.case == "fc1")  # noqa: E731
+        resid = rnd(M, n) if args.case in ("out", "fc2") else None     # the encoder's residual epilogue
+        fn = lambda: wb.linear(a, w, bias=bias, gelu=args.case == "fc1", resid=resid)  # noqa: E731
         flops = 2.0 * M * n * k
     elif args.case == "attention":
         q, k_, v = rnd(B, 1500, d), rnd(B, 1500, d), rnd(B, 1500, d)

@@ -195,8 +195,9 @@ wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8
   g.amap[1] = g.amap[2] = g.amap[3] = g.amap[0];
   if (!b_map(&g.bmap, fp8, W, K, N, 1, K * es, static_cast<uint64_t>(N) * K * es, g.bn)) return WB_ECUDA;
   if (!o_map(&g.omap, out, n_store, M, 1, ldo, static_cast<uint64_t>(M) * ldo)) return WB_ECUDA;
-  g.rmap = g.omap;
-  if (resid && !o_map(&g.rmap, resid, N, M, 1, ldo, static_cast<uint64_t>(M) * ldo)) return WB_ECUDA;
+  p.resid = static_cast<const __nv_bfloat16*>(resid);
+  p.resid_ld = ldo;
+  p.resid_item = static_cast<long long>(M) * ldo;
   p.M = M;
   p.N = N;
   p.batch = 1;
@@ -486,7 +487,6 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     p.n_pass = 3;
     // y1 rows go to rows 1..3000 of each item of y1p [batch][3001][D] (row 0 is the zero pad)
     if (!o_map(&g.omap, y1p, D, N_FRAMES + 1, batch, D, static_cast<uint64_t>(N_FRAMES + 1) * D)) return WB_ECUDA;
-    g.rmap = g.omap;
     p.out_row_off = 1;
     p.bias = w->conv1_b;
     g.p = p;
@@ -515,7 +515,6 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
       p.pass[j] = GemmPass{static_cast<int8_t>(j), 0, 0, static_cast<int8_t>(j), 0, 0, static_cast<int16_t>(D / 64), 0};
     p.n_pass = 3;
     if (!o_map(&g.omap, x0, D, T_TOK, batch, D, static_cast<uint64_t>(T_TOK) * D)) return WB_ECUDA;
-    g.rmap = g.omap;
     p.bias = w->conv2_b;
     g.p = p;
     Prof pr(PC_STEM_CONV2, s);

@@ -13,8 +13,10 @@
 // warps 2-17 run the epilogue of tile i while the MMA warp already
 // accumulates tile i+1.  Epilogue warp w owns TMEM lane quarter w%4 (32 rows)
 // and one quarter of the tile's columns; it stages its 32x32 output boxes in
-// shared memory and writes them with TMA bulk stores (residual boxes arrive
-// the same way).  All waits are bounded.
+// shared memory and writes them with TMA bulk stores.  The residual of the
+// residual epilogue is read with plain 16-byte global loads, one 32-column
+// chunk ahead of its use (the first before the accumulator is ready).  All
+// waits are bounded.
 //
 // K schedule: a list of passes; pass p reads A through tensor map amap[p]
 // (4-D: k, row, part, batch) at row offset a_row_off and part a_part, and B
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap amap0, const __grid_constant__ CUtensorMap amap1,
                 const __grid_constant__ CUtensorMap amap2, const __grid_constant__ CUtensorMap amap3,
                 const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap omap,
-                const __grid_constant__ CUtensorMap rmap, const __grid_constant__ GemmParams p) {
+                const __grid_constant__ GemmParams p) {
   using S = GemmSmem<BN>;
   constexpr int STAGES = S::STAGES;
   constexpr uint32_t IDESC = make_idesc(GEMM_BM, BN, FP8 ? 0u : 1u);
@@ -76,8 +78,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* tfull = bars + 2 * STAGES;         // [2]
   uint64_t* tempty = tfull + 2;                // [2]
   uint64_t* mma_done = tempty + 2;             // [1]
-  uint64_t* rbar = mma_done + 1;               // [GEMM_EPI_WARPS] residual box arrivals
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + GEMM_EPI_WARPS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
@@ -93,7 +94,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(&tempty[a], GEMM_EPI_WARPS);
     }
     mbar_init(mma_done, 1);
-    for (int w = 0; w < GEMM_EPI_WARPS; ++w) mbar_init(&rbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -188,7 +188,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int quarter = warp & 3;                // TMEM lane quarter this warp may access
     const int cg = ew >> 2;                      // column group
     uint8_t* box = smem + S::OFF_EPI + ew * S::EPI_BOX_BYTES;
-    uint32_t rphase = 0;
     bool ok = true;
     int local = 0;
     float alpha_w = 1.0f, alpha_a = 1.0f;
@@ -207,12 +206,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int m = m0 + lane;
       const bool row_ok = m < p.M;
       const int ncol0 = nt * BN + cg * COLS;
-      // residual box of the first chunk: fetch while the accumulator is still being computed
-      if (EPI == EPI_BIAS_RESID && lane == 0 && ncol0 < p.N) {
-        bulk_wait_read0();
-        mbar_arrive_expect_tx(&rbar[ew], S::EPI_BOX_BYTES);
-        tma_load_3d(box, &rmap, &rbar[ew], ncol0, p.out_row_off + m0, b);
-      }
+      // residual of this thread's row, 32 columns (64 bytes) per chunk, loaded one chunk ahead
+      uint4 rnext[4];
+      auto load_resid = [&](int n0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rnext[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (row_ok && n0 < p.N) {
+          const uint4* rp = reinterpret_cast<const uint4*>(
+              p.resid + b * p.resid_item + static_cast<long long>(p.out_row_off + m) * p.resid_ld + n0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) rnext[j] = rp[j];
+        }
+      };
+      if (EPI == EPI_BIAS_RESID) load_resid(ncol0);
       if (!mbar_wait(&tfull[acc], acc_phase, p.err, abort_flag, 4)) { ok = false; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
@@ -226,17 +232,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           alpha = alpha_w * (am > 0.0f ? am / 448.0f : 1.0f);
         }
         float tile_amax = 0.0f;
-        float v[CHUNKS][32];
-#pragma unroll
-        for (int c = 0; c < CHUNKS; ++c) tmem_ld32(t_row + cg * COLS + c * 32, v[c]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is free for tile i+2
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
           const int n0 = ncol0 + c * 32;
-          if (n0 >= p.N) break;
+          float v[32];
+          tmem_ld32(t_row + cg * COLS + c * 32, v);
+          tmem_ld_wait();
+          if (c == CHUNKS - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is free for tile i+2
+          }
+          if (n0 >= p.N) continue;
+          uint4 rcur[4];
+          if (EPI == EPI_BIAS_RESID) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rcur[j] = rnext[j];
+            if (c + 1 < CHUNKS) load_resid(n0 + 32);
+          }
           // bias (+ E4M3 scale) and activation
           const float4* bp = reinterpret_cast<const float4*>(p.bias + n0);
 #pragma unroll
@@ -244,12 +257,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const float4 bb = p.bias ? __ldg(bp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float x = FP8 ? fmaf(v[c][4 * i4 + k], alpha, bv[k]) : v[c][4 * i4 + k] + bv[k];
+            for (int kk = 0; kk < 4; ++kk) {
+              float x = FP8 ? fmaf(v[4 * i4 + kk], alpha, bv[kk]) : v[4 * i4 + kk] + bv[kk];
               if (EPI == EPI_BIAS_GELU || EPI == EPI_CONV2) x = gelu_fast(x);
               if (EPI == EPI_BIAS_RESID && p.act_gelu) x = gelu_fast(x);
-              if (EPI == EPI_CONV2) x += sinusoid(m, n0 + 4 * i4 + k, p.N);
-              v[c][4 * i4 + k] = x;
+              if (EPI == EPI_CONV2) x += sinusoid(m, n0 + 4 * i4 + kk, p.N);
+              v[4 * i4 + kk] = x;
             }
           }
           if (EPI == EPI_BIAS && p.vt && n0 >= p.vt_col0) {
@@ -262,27 +275,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               __half* dst = p.vt + (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
 #pragma unroll
               for (int i = 0; i < 32; ++i)   // f16 for the attention's f16 P.V product (saturated to its range)
-                dst[static_cast<long long>(i) * p.vt_ld] = __float2half_rn(fminf(fmaxf(v[c][i], -65504.0f), 65504.0f));
+                dst[static_cast<long long>(i) * p.vt_ld] = __float2half_rn(fminf(fmaxf(v[i], -65504.0f), 65504.0f));
             }
             continue;
           }
           if (EPI == EPI_BIAS_RESID) {
-            if (!mbar_wait(&rbar[ew], rphase, p.err, abort_flag, 5)) { ok = false; break; }
-            rphase ^= 1u;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint4 u = *reinterpret_cast<const uint4*>(box + box_off(lane, j));
-              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&u);
+              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&rcur[j]);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[c][8 * j + i] += __bfloat162float(hv[i]);
+              for (int i = 0; i < 8; ++i) v[8 * j + i] += __bfloat162float(hv[i]);
             }
-          } else {
-            if (lane == 0) bulk_wait_read0();       // previous store has read the box
-            __syncwarp();
           }
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[c][2 * i], v[c][2 * i + 1]);
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
           if (p.amax && row_ok) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -290,7 +297,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               tile_amax = fmaxf(tile_amax, fmaxf(fabsf(__bfloat162float(hv.x)), fabsf(__bfloat162float(hv.y))));
             }
           }
-          __syncwarp();   // every lane has read the residual box before it is overwritten
+          if (lane == 0) bulk_wait_read0();       // the previous store has read the staging box
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4*>(box + box_off(lane, j)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
@@ -299,12 +307,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (lane == 0) {
             tma_store_3d(&omap, box, n0, p.out_row_off + m0, b);
             bulk_commit();
-            // residual box of the next chunk of this tile goes into the same buffer
-            if (EPI == EPI_BIAS_RESID && c + 1 < CHUNKS && n0 + 32 < p.N) {
-              bulk_wait_read0();
-              mbar_arrive_expect_tx(&rbar[ew], S::EPI_BOX_BYTES);
-              tma_load_3d(box, &rmap, &rbar[ew], n0 + 32, p.out_row_off + m0, b);
-            }
           }
         }
         if (p.amax) {   // one atomic per warp and tile; per lane where the 32 rows straddle two chunks
@@ -375,7 +377,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
 
     if (lane == 0) bulk_wait0();   // stores complete before the CTA (and its smem) goes away
-    if (!ok && EPI == EPI_BIAS_RESID && lane == 0) mbar_drain(&rbar[ew], rphase);
   }
 
   tc_fence_before();

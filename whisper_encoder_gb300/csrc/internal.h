@@ -58,7 +58,6 @@ struct GemmLaunch {
   CUtensorMap amap[GEMM_MAX_AMAPS];
   CUtensorMap bmap;
   CUtensorMap omap;   // output boxes (32 x 32 bf16, 64-byte swizzle), standard epilogues only
-  CUtensorMap rmap;   // residual boxes (EPI_BIAS_RESID)
   GemmParams p;
   int bn;       // 128 or 256
   bool fp8;

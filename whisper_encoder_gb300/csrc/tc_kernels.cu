@@ -58,7 +58,7 @@ cudaError_t gemm_launch_t(const GemmLaunch& g, cudaStream_t s) {
   int grid = sm_count();
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid < 1) return cudaSuccess;
-  kern<<<grid, GEMM_THREADS, smem, s>>>(g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap, g.omap, g.rmap, g.p);
+  kern<<<grid, GEMM_THREADS, smem, s>>>(g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap, g.omap, g.p);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,9 @@ struct GemmParams {
                              // scaled by (amax_a[i] > 0 ? amax_a[i] / 448 : 1) instead of *scale_a
   int rows_per_item;         // rows of one batch item (chunk) in the flattened row index
   int act_gelu;              // EPI_BIAS_RESID only: GELU before the residual add
+  const __nv_bfloat16* resid;  // EPI_BIAS_RESID: residual, element (item, row, n) at
+  long long resid_ld;          //   resid[item * resid_item + (out_row_off + row) * resid_ld + n]
+  long long resid_item;
   float* amax;               // if set: per-item atomic max of |y| (feeds the next E4M3 operand's scale)
   // QKV: columns >= vt_col0 are written transposed, as f16, to vt[(b*H + h)*64 + e][t]
   __half* vt;
