@@ -114,7 +114,8 @@ def test_layernorm_matches_oracle(wb, d, rows):
     assert rel_l2(to_np(y2), oenc.layer_norm(x.astype(np.float64), g, b)) < 4e-3
 
 
-@pytest.mark.parametrize("B,T,H", [(1, 1500, 2), (2, 130, 3), (1, 64, 1), (1, 257, 2)])
+@pytest.mark.parametrize("B,T,H", [(1, 1500, 2), (2, 130, 3), (1, 64, 1), (1, 257, 2), (1, 1, 1), (1, 9, 1),
+                                   (1, 127, 1), (1, 128, 2), (1, 129, 1), (2, 255, 1)])
 def test_attention_matches_oracle(wb, B, T, H):
     rng = np.random.default_rng(T + H)
     d = 64 * H
@@ -135,6 +136,31 @@ def test_attention_peaked_scores(wb):
     v = synthetic.round_to(rng.normal(size=(B, T, 64)).astype(np.float32), "bf16")
     out = to_np(wb.attention(_bf16(q), _bf16(k), _bf16(v), H))
     assert rel_l2(out[0], oenc.attention(q[0].astype(np.float64), k[0], v[0], H)) < 1e-2
+
+
+def test_attention_single_key_returns_v(wb):
+    # T = 1: the only weight is 1 and the row sum is 1, so every output equals v (bf16 -> f16 -> bf16 is exact)
+    rng = np.random.default_rng(5)
+    B, T, H = 3, 1, 4
+    q, k, v = (synthetic.round_to(rng.normal(size=(B, T, 64 * H)).astype(np.float32), "bf16") for _ in range(3))
+    out = to_np(wb.attention(_bf16(q), _bf16(k), _bf16(v), H))
+    assert wb.check_device_error() == 0
+    np.testing.assert_array_equal(out, v)
+
+
+@pytest.mark.parametrize("T", [1000, 1500])
+def test_attention_zero_queries_average_values(wb, T):
+    # q = 0: every score is 0, so each output row is the mean of the value rows over the sequence
+    # (keys past T masked); closed form, independent of the oracle
+    rng = np.random.default_rng(T)
+    B, H = 2, 2
+    q = np.zeros((B, T, 64 * H), np.float32)
+    k, v = (synthetic.round_to(rng.normal(size=(B, T, 64 * H)).astype(np.float32), "bf16") for _ in range(2))
+    out = to_np(wb.attention(_bf16(q), _bf16(k), _bf16(v), H))
+    assert wb.check_device_error() == 0
+    mean = v.astype(np.float64).mean(axis=1, keepdims=True)
+    err = np.abs(out - mean)
+    assert np.all(err <= 2.0 ** -8 * np.abs(mean) + 1e-4), float(err.max())
 
 
 def test_device_error_word_clear(wb):
