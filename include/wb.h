@@ -89,6 +89,12 @@ typedef struct {
   const float* ln2_b;
   const void* w_fc1;  const float* b_fc1;  const float* s_fc1;  /* [F, d],  [F]  */
   const void* w_fc2;  const float* b_fc2;  const float* s_fc2;  /* [d, F],  [d]  */
+  /* Optional LayerNorm folds made by wb_fold_layernorm (all three NULL: not folded).  When a bf16
+   * QKV (FC1) site has them, the forward skips the LN1 (LN2) pass: the GEMM reads the residual
+   * stream itself with w_*_ln and the epilogue applies the row's mean and rstd (see
+   * wb_fold_layernorm).  E4M3 sites ignore them. */
+  const void* w_qkv_ln;  const float* c_qkv;  const float* b_qkv_ln;  /* bf16 [3d, d], f32 [3d], [3d] */
+  const void* w_fc1_ln;  const float* c_fc1;  const float* b_fc1_ln;  /* bf16 [F, d],  f32 [F],  [F]  */
 } wb_layer_weights;
 
 typedef struct {
@@ -190,6 +196,20 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
  * decode(q) * (*scale) as bf16. */
 wb_status wb_quantize_fp8(const void* x, int64_t n, uint8_t* q, float* scale, void* stream);
 wb_status wb_dequantize_fp8(const uint8_t* q, const float* scale, int64_t n, void* y, void* stream);
+
+/* --- LayerNorm folded into the linear layer after it ---------------------------
+ * The pre-LN layer computes y = LN(x; gamma, beta) W^T + b with LN(x) = (x - mean) rstd gamma + beta
+ * (PyPI page, "Direct Kernel API": eps 1e-5).  By that definition
+ *   y[n] = rstd (x . w_ln[n] - mean c[n]) + b_ln[n],  w_ln = W diag(gamma),
+ *   c[n] = sum_k w_ln[n,k],  b_ln[n] = b[n] + sum_k beta[k] W[n,k],
+ * so a GEMM can read x itself and apply the row statistics in its epilogue.  (The pages have no
+ * counterpart: this is a rewrite of the LayerNorm definition, not a step they describe.)
+ * Writes w_ln = bf16(W[n,k] gamma[k]) (bf16 [n_out, d]) and, in float32, c (from the rounded w_ln)
+ * and b_ln ([n_out] each).  w: bf16 [n_out, d]; b may be NULL (zero); gamma, beta: float32 [d].
+ * All pointers are device pointers owned by the caller, 16-byte aligned; d % 8 == 0.
+ * WB_EINVAL for a missing pointer, bad alignment or size. */
+wb_status wb_fold_layernorm(const void* w, const float* b, const float* gamma, const float* beta, int n_out, int d,
+                            void* w_ln, float* c, float* b_ln, void* stream);
 
 /* --- building blocks (exposed for unit tests and custom pipelines) ------------
  * wb_linear: out[m, n] = act(alpha * sum_k a[m, k] w[n, k] + bias[n]) + resid[m, n]

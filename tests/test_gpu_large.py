@@ -14,6 +14,7 @@
     of 36): log-mel of sampled windows <= 1e-3, the final zero-filled window
     through the whole encoder <= 3e-2.
 The oracle runs one chunk at a time in float64 (about 45 s per chunk)."""
+import dataclasses
 import functools
 
 import numpy as np
@@ -88,6 +89,14 @@ def test_large_v3_batch1_per_layer_and_final(wb):
         worst = max(worst, err)
         assert err < 1e-2, (layer, err)
     print(f"worst per-layer relative L2 {worst:.2e}")
+    # the LayerNorm-kernel path (no folds) on the first and last layers
+    enc_plain = wb.EncoderWeights([dataclasses.replace(L, ln_fold={}) for L in enc.layers], enc.ln_post_g,
+                                  enc.ln_post_b)
+    for layer in (0, DIMS.n_layers - 1):
+        h_in = x0_ref if layer == 0 else cap[layer - 1]
+        x = _dev(h_in[None]).to(torch.bfloat16)
+        h = to_np(wb.encoder_forward(x, DIMS, enc_plain, layer_begin=layer, layer_end=layer + 1, final_ln=False))[0]
+        assert rel_l2(h, cap[layer]) < 1e-2, layer
 
 
 @pytest.fixture(scope="module")

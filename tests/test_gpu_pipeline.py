@@ -2,6 +2,8 @@
 log-mel (max abs <= 1e-3), conv stem, encoder layers (relative L2 <= 1e-2 per
 layer, <= 3e-2 after the final LayerNorm, <= 6e-2 for mixed_fp8), on the
 seeded synthetic workloads."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -78,6 +80,46 @@ def test_tiny_pipeline_matches_oracle(wb):
     h = to_np(wb.encoder_forward(x0, dims, enc, final_ln=False))[0]
     ref_h = oenc.encoder(to_np(x0)[0], w, dims.n_heads, final_ln=False)
     assert rel_l2(h, ref_h) < LAYER_TOL
+
+
+def _unfolded(wb, enc):
+    """The same device weights without the LayerNorm folds: every site runs its LayerNorm pass."""
+    return wb.EncoderWeights([dataclasses.replace(L, ln_fold={}) for L in enc.layers], enc.ln_post_g, enc.ln_post_b)
+
+
+def test_fold_layernorm_weights(wb):
+    # w_ln = bf16(W diag(gamma)) bitwise; c = row sums of w_ln; b_ln = b + W beta
+    rng = np.random.default_rng(21)
+    n, d = 384, 256
+    w = torch.from_numpy(rng.normal(0, 0.02, size=(n, d)).astype(np.float32)).to(DEV).to(torch.bfloat16)
+    b = torch.from_numpy(rng.normal(0, 0.02, size=n).astype(np.float32)).to(DEV)
+    gam = torch.from_numpy((1 + rng.normal(0, 0.02, size=d)).astype(np.float32)).to(DEV)
+    bet = torch.from_numpy(rng.normal(0, 0.02, size=d).astype(np.float32)).to(DEV)
+    w_ln, c, b_ln = wb.fold_layernorm(w, b, gam, bet)
+    assert torch.equal(w_ln, (w.float() * gam[None, :]).to(torch.bfloat16))
+    w64, wl64 = to_np(w).astype(np.float64), to_np(w_ln).astype(np.float64)
+    np.testing.assert_allclose(to_np(c), wl64.sum(1), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(to_np(b_ln), to_np(b) + w64 @ to_np(bet), rtol=1e-5, atol=1e-6)
+    _, c0, b0 = wb.fold_layernorm(w, None, gam, bet)             # no bias
+    np.testing.assert_allclose(to_np(b0), w64 @ to_np(bet), rtol=1e-5, atol=1e-6)
+
+
+def test_tiny_folded_and_unfolded_layernorm_agree_with_oracle(wb):
+    # the folded path (GEMM on the residual stream, row statistics in the epilogue) and the
+    # LayerNorm-kernel path both match the oracle, and each other
+    dims, w = _tiny()
+    _, enc = wb.upload_weights(w)
+    assert all(set(L.ln_fold) == {"w_qkv", "w_fc1"} for L in enc.layers)
+    x0 = oenc.conv_stem(ofe.log_mel(synthetic.tone_chunk(9), dims.n_mels), w)
+    x0d = _dev(np.stack([x0, x0[::-1]])).to(torch.bfloat16)
+    folded = to_np(wb.encoder_forward(x0d, dims, enc, final_ln=False))
+    plain = to_np(wb.encoder_forward(x0d, dims, _unfolded(wb, enc), final_ln=False))
+    assert wb.check_device_error() == 0
+    for b in range(2):
+        ref = oenc.encoder(to_np(x0d)[b], w, dims.n_heads, final_ln=False)
+        assert rel_l2(folded[b], ref) < LAYER_TOL
+        assert rel_l2(plain[b], ref) < LAYER_TOL
+        assert rel_l2(folded[b], plain[b]) < LAYER_TOL
 
 
 def test_tiny_mixed_fp8(wb):

@@ -36,7 +36,8 @@ class wb_stem_weights(ctypes.Structure):
 class wb_layer_weights(ctypes.Structure):
     _fields_ = [(n, c_void) for n in (
         "ln1_g", "ln1_b", "w_qkv", "b_qkv", "s_qkv", "w_out", "b_out", "s_out", "ln2_g", "ln2_b",
-        "w_fc1", "b_fc1", "s_fc1", "w_fc2", "b_fc2", "s_fc2")]
+        "w_fc1", "b_fc1", "s_fc1", "w_fc2", "b_fc2", "s_fc2",
+        "w_qkv_ln", "c_qkv", "b_qkv_ln", "w_fc1_ln", "c_fc1", "b_fc1_ln")]
 
 
 class wb_cross_kv_weights(ctypes.Structure):
@@ -62,6 +63,7 @@ SIGNATURES = {
     "wb_encoder_forward": (c_int, [c_void, c_int, P(wb_dims), P(wb_layer_weights), P(wb_ln_weights),
                                    P(wb_precision), c_int, c_int, c_int, c_void, c_void, c_size, c_void]),
     "wb_quantize_fp8": (c_int, [c_void, c_i64, c_void, c_void, c_void]),
+    "wb_fold_layernorm": (c_int, [c_void, c_void, c_void, c_void, c_int, c_int, c_void, c_void, c_void, c_void]),
     "wb_dequantize_fp8": (c_int, [c_void, c_void, c_i64, c_void, c_void]),
     "wb_linear": (c_int, [c_void, c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void, c_int, c_void,
                           c_void, c_void]),

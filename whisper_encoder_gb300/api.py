@@ -142,6 +142,18 @@ def quantize_fp8(x: torch.Tensor, stream=None):
     return q, scale
 
 
+def fold_layernorm(w: torch.Tensor, b, gamma: torch.Tensor, beta: torch.Tensor, stream=None):
+    """LayerNorm (gamma, beta) folded into the linear layer (w bf16 [n, d], b f32 [n] or None) after it:
+    returns (w_ln bf16 [n, d], c f32 [n], b_ln f32 [n]) for wb_encoder_forward's folded sites."""
+    _need(w, torch.bfloat16, "w")
+    n, d = w.shape
+    w_ln = torch.empty_like(w)
+    c = torch.empty(n, dtype=torch.float32, device=w.device)
+    b_ln = torch.empty(n, dtype=torch.float32, device=w.device)
+    call("wb_fold_layernorm", _p(w), _p(b), _p(gamma), _p(beta), n, d, _p(w_ln), _p(c), _p(b_ln), _stream(stream))
+    return w_ln, c, b_ln
+
+
 def dequantize_fp8(q: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:
     _need(q, torch.uint8, "q")
     y = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
@@ -272,6 +284,7 @@ class LayerWeights:
     w_fc2: torch.Tensor
     b_fc2: torch.Tensor
     fp8: dict = dataclasses.field(default_factory=dict)   # name -> (codes, scale) for E4M3 copies
+    ln_fold: dict = dataclasses.field(default_factory=dict)   # "w_qkv" / "w_fc1" -> (w_ln, c, b_ln)
 
 
 @dataclasses.dataclass
@@ -286,6 +299,15 @@ class EncoderWeights:
             for n in names:
                 if n not in L.fp8:
                     L.fp8[n] = quantize_fp8(getattr(L, n))
+
+    def fold_layernorm(self):
+        """Fold LN1 into the QKV weights and LN2 into the FC1 weights of every layer (bf16 sites then
+        skip their LayerNorm pass)."""
+        for L in self.layers:
+            if "w_qkv" not in L.ln_fold:
+                L.ln_fold["w_qkv"] = fold_layernorm(L.w_qkv, L.b_qkv, L.ln1_g, L.ln1_b)
+            if "w_fc1" not in L.ln_fold:
+                L.ln_fold["w_fc1"] = fold_layernorm(L.w_fc1, L.b_fc1, L.ln2_g, L.ln2_b)
 
     def layer_array(self, precision):
         qkv8, out8, ffn8 = precision[0] == WB_E4M3, precision[2] == WB_E4M3, precision[4] == WB_E4M3
@@ -302,15 +324,20 @@ class EncoderWeights:
             wo, so = pick("w_out", out8)
             w1, s1 = pick("w_fc1", ffn8)
             w2, s2 = pick("w_fc2", ffn8)
+            def fold(name):
+                f = L.ln_fold.get(name)
+                return tuple(t.data_ptr() for t in f) if f is not None else (None, None, None)
             arr[i] = _lib.wb_layer_weights(L.ln1_g.data_ptr(), L.ln1_b.data_ptr(), wq, L.b_qkv.data_ptr(), sq,
                                            wo, L.b_out.data_ptr(), so, L.ln2_g.data_ptr(), L.ln2_b.data_ptr(),
-                                           w1, L.b_fc1.data_ptr(), s1, w2, L.b_fc2.data_ptr(), s2)
+                                           w1, L.b_fc1.data_ptr(), s1, w2, L.b_fc2.data_ptr(), s2,
+                                           *fold("w_qkv"), *fold("w_fc1"))
         self._arr = arr
         return arr
 
 
-def upload_weights(w: dict, device="cuda"):
-    """Host weight dict (HF layout, float32 arrays) -> (StemWeights, EncoderWeights) on the device."""
+def upload_weights(w: dict, device="cuda", fold_ln: bool = True):
+    """Host weight dict (HF layout, float32 arrays) -> (StemWeights, EncoderWeights) on the device.
+    fold_ln: also make the LayerNorm folds of every layer (EncoderWeights.fold_layernorm)."""
     def f32(a):
         return torch.as_tensor(a, dtype=torch.float32).to(device).contiguous()
 
@@ -329,6 +356,8 @@ def upload_weights(w: dict, device="cuda"):
             f32(L["ln1_g"]), f32(L["ln1_b"]), bf16(w_qkv), f32(b_qkv), bf16(L["wo"]), f32(L["bo"]),
             f32(L["ln2_g"]), f32(L["ln2_b"]), bf16(L["w1"]), f32(L["b1"]), bf16(L["w2"]), f32(L["b2"])))
     enc = EncoderWeights(layers, f32(w["ln_post_g"]), f32(w["ln_post_b"]))
+    if fold_ln:
+        enc.fold_layernorm()
     return stem, enc
 
 

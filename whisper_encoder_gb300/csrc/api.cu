@@ -220,7 +220,7 @@ bool dims_ok(const wb_dims* d) {
 bool site_ok(int w, int a) { return (w == WB_BF16 || w == WB_E4M3) && w == a; }
 
 struct EncLayout {
-  size_t h, a, qk, vt, o, g, aq, gq, slots, total;
+  size_t h, a, qk, vt, o, g, aq, gq, slots, stats, total;
 };
 
 EncLayout enc_layout(const wb_dims* d, int batch, const wb_precision* pr) {
@@ -240,6 +240,8 @@ EncLayout enc_layout(const wb_dims* d, int batch, const wb_precision* pr) {
   L.gq = ffn8 ? c.take(M * F) : 0;
   // per layer, per E4M3 operand site (qkv, out, fc1, fc2 inputs), per batch item: one absmax
   L.slots = c.take(static_cast<size_t>(4) * (d->n_layers > 0 ? d->n_layers : 1) * batch * sizeof(float));
+  // LayerNorm row statistics (mean, rstd) for a folded LN1 / LN2 site
+  L.stats = c.take(M * sizeof(float2));
   L.total = c.off;
   return L;
 }
@@ -570,6 +572,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
                  : nullptr;
   auto* gq = pr.ffn_a == WB_E4M3 ? reinterpret_cast<uint8_t*>(ws + EL.gq) : nullptr;
   auto* slots = reinterpret_cast<float*>(ws + EL.slots);
+  auto* stats = reinterpret_cast<float2*>(ws + EL.stats);
   const auto* x0b = static_cast<const __nv_bfloat16*>(x0);
   auto* outb = static_cast<__nv_bfloat16*>(out);
   const float eps = 1e-5f;
@@ -577,6 +580,13 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
 
   if (n_layers_run > 0 && (pr.qkv_a == WB_E4M3 || pr.out_a == WB_E4M3 || pr.ffn_a == WB_E4M3))
     WB_CUDA(cudaMemsetAsync(slots, 0, sizeof(float) * 4 * dims->n_layers * batch, s));
+  // a bf16 site whose LayerNorm is folded into its GEMM reads the row statistics instead of LN's output
+  auto fold_qkv = [&](int l) {
+    return pr.qkv_a == WB_BF16 && layers[l].w_qkv_ln && layers[l].c_qkv && layers[l].b_qkv_ln;
+  };
+  auto fold_fc1 = [&](int l) {
+    return pr.ffn_a == WB_BF16 && layers[l].w_fc1_ln && layers[l].c_fc1 && layers[l].b_fc1_ln;
+  };
 
   for (int l = layer_begin; l < layer_end; ++l) {
     const wb_layer_weights& W = layers[l];
@@ -589,10 +599,14 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     const bool last = (l == layer_end - 1);
     const bool q8 = pr.qkv_a == WB_E4M3, o8 = pr.out_a == WB_E4M3, f8 = pr.ffn_a == WB_E4M3;
 
-    // LN1 -> a  [-> E4M3]
+    const bool fq = fold_qkv(l), ff = fold_fc1(l);
+    // LN1 -> a  [-> E4M3]  (folded: only the row statistics; QKV reads src itself)
     {
       Prof pr(PC_ENC_LN, s);
-      WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? am_qkv : nullptr, T_TOK, s));
+      if (fq)
+        WB_CUDA(launch_ln_stats(src, M, D, eps, stats, s));
+      else
+        WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? am_qkv : nullptr, T_TOK, s));
     }
     if (q8) {
       Prof pr(PC_ENC_QUANT, s);
@@ -609,8 +623,16 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.amax_a = am_qkv;
         p.scale_b = W.s_qkv;
       }
-      wb_status st = dense_gemm(q8 ? static_cast<const void*>(aq) : a, W.w_qkv, M, 3 * D, D, q8, EPI_BIAS, qk, 2 * D,
-                                2 * D, nullptr, p, s, PC_ENC_QKV);
+      const void* qkv_a = q8 ? static_cast<const void*>(aq) : static_cast<const void*>(a);
+      const void* qkv_w = W.w_qkv;
+      if (fq) {
+        p.bias = W.b_qkv_ln;
+        p.ln_stats = stats;
+        p.ln_c = W.c_qkv;
+        qkv_a = src;
+        qkv_w = W.w_qkv_ln;
+      }
+      wb_status st = dense_gemm(qkv_a, qkv_w, M, 3 * D, D, q8, EPI_BIAS, qk, 2 * D, 2 * D, nullptr, p, s, PC_ENC_QKV);
       if (st != WB_OK) return st;
     }
     {
@@ -633,8 +655,11 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
                                 src, p, s, PC_ENC_OUT);
       if (st != WB_OK) return st;
     }
-    // LN2 -> a [-> E4M3]
-    {
+    // LN2 -> a [-> E4M3]  (folded: only the row statistics; FC1 reads h itself)
+    if (ff) {
+      Prof pr(PC_ENC_LN, s);
+      WB_CUDA(launch_ln_stats(h, M, D, eps, stats, s));
+    } else {
       Prof pr(PC_ENC_LN, s);
       WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? am_fc1 : nullptr, T_TOK, s));
     }
@@ -650,8 +675,16 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.scale_b = W.s_fc1;
         p.amax = am_fc2;
       }
-      wb_status st = dense_gemm(f8 ? static_cast<const void*>(aq) : a, W.w_fc1, M, F, D, f8, EPI_BIAS_GELU, g, F, F,
-                                nullptr, p, s, PC_ENC_FC1);
+      const void* fc1_a = f8 ? static_cast<const void*>(aq) : static_cast<const void*>(a);
+      const void* fc1_w = W.w_fc1;
+      if (ff) {
+        p.bias = W.b_fc1_ln;
+        p.ln_stats = stats;
+        p.ln_c = W.c_fc1;
+        fc1_a = h;
+        fc1_w = W.w_fc1_ln;
+      }
+      wb_status st = dense_gemm(fc1_a, fc1_w, M, F, D, f8, EPI_BIAS_GELU, g, F, F, nullptr, p, s, PC_ENC_FC1);
       if (st != WB_OK) return st;
     }
     if (f8) {
@@ -701,6 +734,19 @@ wb_status wb_dequantize_fp8(const uint8_t* q, const float* scale, int64_t n, voi
   if (n == 0) return WB_OK;
   if (!q || !y) return WB_EINVAL;
   WB_CUDA(launch_dequantize(q, scale, n, static_cast<__nv_bfloat16*>(y), static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+wb_status wb_fold_layernorm(const void* w, const float* b, const float* gamma, const float* beta, int n_out, int d,
+                            void* w_ln, float* c, float* b_ln, void* stream) {
+  if (n_out < 0 || d <= 0 || d % 8) return WB_EINVAL;
+  if (n_out == 0) return WB_OK;
+  if (!w || !gamma || !beta || !w_ln || !c || !b_ln) return WB_EINVAL;
+  if (!aligned16(w) || !aligned16(w_ln) || !aligned16(gamma) || !aligned16(beta) || (b && !aligned16(b)) ||
+      !aligned16(c) || !aligned16(b_ln))
+    return WB_EINVAL;
+  WB_CUDA(launch_fold_ln(static_cast<const __nv_bfloat16*>(w), b, gamma, beta, n_out, d,
+                         static_cast<__nv_bfloat16*>(w_ln), c, b_ln, static_cast<cudaStream_t>(stream)));
   return WB_OK;
 }
 

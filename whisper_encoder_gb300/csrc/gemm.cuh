@@ -219,6 +219,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       };
       if (EPI == EPI_BIAS_RESID) load_resid(ncol0);
+      // folded LayerNorm: this row's (mean, rstd), fetched while the accumulator is still being computed
+      const bool lnf = (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) && !FP8 && p.ln_stats != nullptr;
+      float2 ln_mr = make_float2(0.0f, 1.0f);
+      if (lnf && row_ok) ln_mr = p.ln_stats[static_cast<long long>(b) * p.M + m];
       if (!mbar_wait(&tfull[acc], acc_phase, p.err, abort_flag, 4)) { ok = false; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
@@ -232,6 +236,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           alpha = alpha_w * (am > 0.0f ? am / 448.0f : 1.0f);
         }
         float tile_amax = 0.0f;
+        const float ln_mu = ln_mr.x, ln_rs = ln_mr.y;
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
           const int n0 = ncol0 + c * 32;
@@ -252,13 +257,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           // bias (+ E4M3 scale) and activation
           const float4* bp = reinterpret_cast<const float4*>(p.bias + n0);
+          const float4* cp = reinterpret_cast<const float4*>(p.ln_c + n0);
 #pragma unroll
           for (int i4 = 0; i4 < 8; ++i4) {
             const float4 bb = p.bias ? __ldg(bp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+            const float4 c4 = lnf ? __ldg(cp + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               float x = FP8 ? fmaf(v[4 * i4 + kk], alpha, bv[kk]) : v[4 * i4 + kk] + bv[kk];
+              if (lnf) x = fmaf(ln_rs, fmaf(-ln_mu, cv[kk], v[4 * i4 + kk]), bv[kk]);
               if (EPI == EPI_BIAS_GELU || EPI == EPI_CONV2) x = gelu_fast(x);
               if (EPI == EPI_BIAS_RESID && p.act_gelu) x = gelu_fast(x);
               if (EPI == EPI_CONV2) x += sinusoid(m, n0 + 4 * i4 + kk, p.N);

@@ -34,6 +34,9 @@ cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, c
                              int rows_per_item, cudaStream_t s);
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
                            float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s);
+cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s);
+cudaError_t launch_fold_ln(const __nv_bfloat16* w, const float* b, const float* gamma, const float* beta, int n_out,
+                           int d, __nv_bfloat16* w_ln, float* c, float* b_ln, cudaStream_t s);
 cudaError_t launch_quantize_e5m2(const __nv_bfloat16* x, long long n, uint8_t* q, float* amax_to_scale,
                                  cudaStream_t s);
 cudaError_t launch_dequantize_e5m2(const uint8_t* q, const float* scale, long long n, __nv_bfloat16* y,

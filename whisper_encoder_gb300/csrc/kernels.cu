@@ -298,6 +298,85 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 }
 
 // ---------------------------------------------------------------------------
+// LayerNorm folded into the following GEMM.  For y = LN(x; gamma, beta) W^T + b with
+// LN(x) = (x - mean) rstd gamma + beta:
+//   y[n] = rstd (sum_k x[k] W[n,k] gamma[k] - mean sum_k W[n,k] gamma[k]) + b[n] + sum_k beta[k] W[n,k],
+// an identity of the LayerNorm definition.  The GEMM then reads x itself with B = W diag(gamma).
+// ---------------------------------------------------------------------------
+
+// (mean, rstd) of every row of x (bf16 [rows, d]) as LayerNorm computes them (two passes over the
+// row in registers, rstd = 1 / sqrt(var + eps)); warp per row, 16-byte loads, no output rows.
+constexpr int STATS_MAXC = 8;                  // 16-byte chunks per lane: d <= 8 * 32 * 8 = 2048
+__global__ void ln_row_stats_kernel(const __nv_bfloat16* __restrict__ x, long long rows, int d, float eps,
+                                    float2* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const long long warp_g = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const int nc = d / 8;
+  for (long long row = warp_g; row < rows; row += n_warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * d);
+    uint4 u[STATS_MAXC];
+    float s1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < STATS_MAXC; ++i) {
+      if (lane + 32 * i < nc) {
+        u[i] = src[lane + 32 * i];
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s1 += __bfloat162float(h[j]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    const float mean = s1 / static_cast<float>(d);
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < STATS_MAXC; ++i) {
+      if (lane + 32 * i < nc) {
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u[i]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float t = __bfloat162float(h[j]) - mean;
+          q = fmaf(t, t, q);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    if (lane == 0) out[row] = make_float2(mean, rsqrtf(q / static_cast<float>(d) + eps));
+  }
+}
+
+// w_ln[n,k] = bf16(w[n,k] gamma[k]); c[n] = sum_k w_ln[n,k]; b_ln[n] = b[n] + sum_k beta[k] w[n,k].
+// One warp per output row, lanes striding over k, fixed-order shuffle reduction (deterministic).
+__global__ void fold_ln_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ b,
+                               const float* __restrict__ gamma, const float* __restrict__ beta, int n_out, int d,
+                               __nv_bfloat16* __restrict__ w_ln, float* __restrict__ c, float* __restrict__ b_ln) {
+  const long long n = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (n >= n_out) return;
+  const __nv_bfloat16* wr = w + n * d;
+  __nv_bfloat16* orow = w_ln + n * d;
+  float sc = 0.0f, sb = 0.0f;
+  for (int k = lane; k < d; k += 32) {
+    const float wv = __bfloat162float(wr[k]);
+    const __nv_bfloat16 f = __float2bfloat16_rn(wv * gamma[k]);
+    orow[k] = f;
+    sc += __bfloat162float(f);
+    sb = fmaf(beta[k], wv, sb);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sc += __shfl_xor_sync(0xffffffffu, sc, o);
+    sb += __shfl_xor_sync(0xffffffffu, sb, o);
+  }
+  if (lane == 0) {
+    c[n] = sc;
+    b_ln[n] = (b ? b[n] : 0.0f) + sb;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // FP8 E4M3 per-tensor scaling.
 // ---------------------------------------------------------------------------
 __global__ void amax_kernel(const __nv_bfloat16* __restrict__ x, long long n, float* __restrict__ amax) {
@@ -582,6 +661,22 @@ cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, c
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
                            float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s) {
   return norm_dispatch<true>(x, res, g, nullptr, rows, d, eps, y, total, nullptr, 0, s);
+}
+
+cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s) {
+  if (d <= 0 || d % 8 || d > STATS_MAXC * 32 * 8) return cudaErrorInvalidValue;
+  if (rows == 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;               // 8 warps per block, a warp per row
+  ln_row_stats_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(x, rows, d, eps, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_ln(const __nv_bfloat16* w, const float* b, const float* gamma, const float* beta, int n_out,
+                           int d, __nv_bfloat16* w_ln, float* c, float* b_ln, cudaStream_t s) {
+  const long long threads = static_cast<long long>(n_out) * 32;
+  if (threads == 0) return cudaSuccess;
+  fold_ln_kernel<<<static_cast<int>((threads + 255) / 256), 256, 0, s>>>(w, b, gamma, beta, n_out, d, w_ln, c, b_ln);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaStream_t s) {

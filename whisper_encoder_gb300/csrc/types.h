@@ -50,6 +50,11 @@ struct GemmParams {
   const __nv_bfloat16* resid;  // EPI_BIAS_RESID: residual, element (item, row, n) at
   long long resid_ld;          //   resid[item * resid_item + (out_row_off + row) * resid_ld + n]
   long long resid_item;
+  // EPI_BIAS / EPI_BIAS_GELU, bf16: a LayerNorm folded into this GEMM.  A is the un-normalised row x,
+  // B = W diag(gamma), ln_stats[r] = (mean, rstd) of flattened row r = b*M + m, and the epilogue
+  // forms rstd (acc - mean ln_c[n]) + bias[n]
+  const float2* ln_stats;
+  const float* ln_c;
   float* amax;               // if set: per-item atomic max of |y| (feeds the next E4M3 operand's scale)
   // QKV: columns >= vt_col0 are written transposed, as f16, to vt[(b*H + h)*64 + e][t]
   __half* vt;
