@@ -396,10 +396,54 @@ class Pipeline:
         return graph
 
     def __call__(self, audio: torch.Tensor, chunk_stride: int = CHUNK_SAMPLES, n_chunks: int | None = None,
-                 stream=None) -> torch.Tensor:
+                 stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
         n = self.batch if n_chunks is None else n_chunks
+        dst = self.out if out is None else out
         logmel(audio, n, self.dims.n_mels, chunk_stride, out=self.mel[:n], workspace=self.ws_mel, stream=stream)
         conv_stem(self.mel[:n], self.dims, self.stem, out=self.x0[:n], workspace=self.ws_stem, stream=stream)
-        encoder_forward(self.x0[:n], self.dims, self.enc, self.precision, out=self.out[:n], workspace=self.ws_enc,
+        encoder_forward(self.x0[:n], self.dims, self.enc, self.precision, out=dst[:n], workspace=self.ws_enc,
                         stream=stream)
-        return self.out[:n]
+        return dst[:n]
+
+    def run_host(self, host_in: list, host_out: list, chunk_stride: int = CHUNK_SAMPLES) -> None:
+        """Encode a sequence of full batches held in pinned host memory.
+
+        host_in[i]: pinned float32 audio of batch i (as for __call__); host_out[i]: pinned bf16
+        [batch, 1500, d] that receives batch i's encoder output.  Batch i's audio upload and result
+        download run on two copy streams, against two device input and two device output buffers,
+        so they overlap the compute of batches i-1 and i+1.  Returns with all work queued on the
+        current stream (synchronize it to wait for the last download)."""
+        comp = torch.cuda.current_stream()
+        if not hasattr(self, "_copy"):
+            self._copy = (torch.cuda.Stream(), torch.cuda.Stream())
+            self._out2 = torch.empty_like(self.out)
+            self._dev_in = None
+        up, down = self._copy
+        if self._dev_in is None or self._dev_in[0].shape != host_in[0].shape:
+            self._dev_in = [torch.empty(host_in[0].shape, dtype=torch.float32, device=self.out.device) for _ in range(2)]
+        outs = (self.out, self._out2)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        in_free = [torch.cuda.Event() for _ in range(2)]
+        out_ready = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+        up.wait_stream(comp)
+        down.wait_stream(comp)
+        for i, (hi, ho) in enumerate(zip(host_in, host_out)):
+            k = i % 2
+            if i >= 2:
+                up.wait_event(in_free[k])              # the compute that read this buffer is done
+            with torch.cuda.stream(up):
+                self._dev_in[k].copy_(hi, non_blocking=True)
+            in_ready[k].record(up)
+            comp.wait_event(in_ready[k])
+            if i >= 2:
+                comp.wait_event(out_free[k])           # the download of this output buffer is done
+            self(self._dev_in[k], chunk_stride, out=outs[k])
+            in_free[k].record(comp)
+            out_ready[k].record(comp)
+            down.wait_event(out_ready[k])
+            with torch.cuda.stream(down):
+                ho.copy_(outs[k], non_blocking=True)
+            out_free[k].record(down)
+        comp.wait_stream(down)
+        comp.wait_stream(up)
