@@ -94,6 +94,11 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.wb_layernorm(fake, None, fake, fake, 4, 200, 1e-5, fake, None, None) == _lib.WB_EINVAL
     assert lib.wb_attention(fake, fake, fake, 1, 1505, 2, fake, fake, 1 << 30, None) == _lib.WB_EINVAL
     assert lib.wb_quantize_fp8(fake, -1, fake, fake, None) == _lib.WB_EINVAL
+    # LayerNorm fold: width not a multiple of 8, missing gamma, misaligned output, nothing to do
+    assert lib.wb_fold_layernorm(fake, None, fake, fake, 16, 12, fake, fake, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_fold_layernorm(fake, None, None, fake, 16, 64, fake, fake, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_fold_layernorm(fake, None, fake, fake, 16, 64, odd, fake, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_fold_layernorm(None, None, None, None, 0, 64, None, None, None, None) == _lib.WB_OK
 
 
 def _imports(path):
