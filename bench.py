@@ -56,11 +56,33 @@ def flops_per_chunk(dims) -> dict:
     }
 
 
-def bytes_per_chunk(dims) -> dict:
-    """Algorithmic HBM bytes of the bandwidth-bound classes per chunk."""
-    T, d = 1500, dims.d_model
+def bytes_per_chunk(dims, precision: str = "bf16") -> dict:
+    """Algorithmic HBM bytes of the bandwidth-bound classes per chunk (bf16 activations)."""
+    T, d, F, C = 1500, dims.d_model, dims.d_ffn, dims.n_mels
     L = dims.n_layers
-    return {"enc.layernorm": (2 * L + 1) * T * d * 2 * 2.0}
+    row = T * d * 2.0                                   # one [1500, d] bf16 tensor
+    out = {"logmel.post": 2.0 * C * 3000 * 4,           # clamp + scale in place
+           "logmel.prep": 480000 * 4 + 3 * 480400 * 2.0}   # audio in, padded split-bf16 copy out
+    if precision == "bf16":
+        # LN1 / LN2 folded into QKV / FC1: the statistics kernels read each row once; the final LN reads + writes
+        out["enc.layernorm"] = 2 * L * row + 2 * row
+    else:
+        out["enc.layernorm"] = (2 * L + 1) * 2 * row    # every LN reads and writes
+        # E4M3 copies of the QKV and FC1 inputs ([1500, d]) and of the FC2 input ([1500, F]): read bf16, write u8
+        out["enc.quantize"] = L * (2 * (row + row / 2) + (T * F * 2.0 + T * F))
+    return out
+
+
+def step_roofline(fl: dict, by: dict, B: int, peaks: dict, fp8_classes: set, ms_step: float) -> dict:
+    """Roofline time of one step: sum over kernel classes of max(FLOPs / peak, bytes / HBM bandwidth)."""
+    t = 0.0
+    for c in set(fl) | set(by):
+        tf = fl.get(c, 0.0) * B / (peaks["bf16_sustained"] * 1e12 * (2.0 if c in fp8_classes else 1.0))
+        tb = by.get(c, 0.0) * B / (peaks["hbm_gbs"] * 1e9)
+        t += max(tf, tb)
+    return {"ideal_ms": round(t * 1e3, 3), "frac": round(t * 1e3 / ms_step, 4),
+            "peaks": f"{peaks['source']}: bf16 sustained {peaks['bf16_sustained']} TFLOP/s (x2 for E4M3 GEMM "
+                     f"classes), HBM {peaks['hbm_gbs']} GB/s"}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture of the
@@ -164,6 +186,13 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_info() -> dict:
+    """Host threads the oracle may use: all cores, the affinity mask, the BLAS thread setting."""
+    blas = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS") if k in os.environ}
+    return {"os_cpu_count": os.cpu_count(), "affinity_cpus": cpu_cores(),
+            "blas_threads": blas or "library default (all cores)"}
+
+
 def run_reference(args) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -184,7 +213,8 @@ def run_reference(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000.0, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": arm_config(args, 1),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample,
+                         "host": cpu_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -243,6 +273,32 @@ def run_case(args) -> None:
         bet = torch.zeros(d, device="cuda")
         fn = lambda: wb.layernorm(x, gam, bet)  # noqa: E731
         flops = 2.0 * M * d * 2      # bytes moved (read + write), reported in the same field
+    elif args.case == "longform":
+        # 45 min of synthetic audio in 30 s windows at a 25 s stride (the PyPI page's overlapping-chunk
+        # mode): 108 windows through the same three calls in 3 batches of 36, audio already on the device
+        stride, per = 400000, 36
+        x = synthetic.long_audio(synthetic.SEED_LONGFORM)
+        n = 1 + max(0, -(-(len(x) - 480000) // stride))
+        stem, enc = wb.upload_weights(synthetic.encoder_weights(dims, synthetic.SEED_LONGFORM, "bf16"))
+        xd = torch.from_numpy(x).cuda()
+        pipe = wb.Pipeline(dims, stem, enc, batch=per)
+
+        def fn():
+            for i in range(0, n, per):
+                pipe(xd[i * stride:], chunk_stride=stride, n_chunks=min(per, n - i))
+        fn()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(3):
+            fn()
+        ev[1].record()
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[1]) / 3
+        audio_s = len(x) / 16000.0
+        print(json.dumps({"case": "longform", "windows": n, "audio_s": audio_s, "ms": round(ms, 3),
+                          "audio_s_per_s": round(audio_s / (ms / 1000.0), 1)}))
+        return
     elif args.case == "logmel":
         audio = torch.randn(B * 480000, device="cuda", generator=g) * 0.1
         fn = lambda: wb.logmel(audio, B, dims.n_mels)  # noqa: E731
@@ -274,7 +330,8 @@ def main() -> None:
     ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph of the three calls")
-    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "logmel"), default=None,
+    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "logmel", "longform"),
+                    default=None,
                     help="launch one kernel class at full size (for profiler captures) instead of the bench")
     args = ap.parse_args()
     if args.case:
@@ -417,6 +474,7 @@ def main() -> None:
                     "peak_source": f"{peaks['source']} bf16 sustained"
                                    + (" x2 (E4M3 nominal ratio)" if dom in fp8_classes else "")}
     step_flops = sum(fl.values()) * B
+    step_roof = step_roofline(fl, bytes_per_chunk(dims, args.precision), B, peaks, fp8_classes, ms_step)
     # launches per step: counted by the library's own events (eager), or one graph launch
     gpu_launches = sum(n for _, n in prof.values()) if prof else graph_launches * args.steps
 
@@ -427,13 +485,13 @@ def main() -> None:
         "impl": "wb",
         "config": arm_config(args, world),
         "tflops": round(step_flops / (ms_step / 1000.0) / 1e12, 1),
-        "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "graph": bool(args.graph),
+        "roofline": roofline, "step_roofline": step_roof, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "graph": bool(args.graph),
         "kernels": kernels,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, parts = oracle_chunk_seconds(dims, seed)
         line["cpu_baseline"] = {
-            "value": round(CHUNK_S / t, 5), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "value": round(CHUNK_S / t, 5), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "host": cpu_info(),
             "sample": ("1 chunk of 30 s through the float64 oracle's log-mel, conv stem, 1 of 32 layers and one "
                        "LayerNorm; per-chunk time extrapolated to 32 layers"),
             "parts_s": {k: round(v, 3) for k, v in parts.items()}}
