@@ -116,6 +116,18 @@ int wb_version(void);
  * *detail (optional) receives the raw word (bits 8..15: the wait site). */
 wb_status wb_check_device_error(void* stream, uint32_t* detail);
 
+/* Wait site that wb_selftest_wait_timeout() records (bits 8..15 of the word). */
+#define WB_SELFTEST_WAIT_SITE 0x7Fu
+
+/* Diagnostic of the bounded-wait path (no compute).  Launches one kernel on
+ * `stream` whose single thread waits on an mbarrier that nothing arrives on.
+ * The wait gives up after its time limit (about 2 s), sets the timeout bit and
+ * WB_SELFTEST_WAIT_SITE in the device error word, and the kernel returns
+ * normally: the context stays usable.  The next wb_check_device_error() then
+ * returns WB_ETIMEOUT and clears the word.  Returns WB_ECUDA if the launch
+ * fails, else WB_OK (asynchronously; nothing else is touched). */
+wb_status wb_selftest_wait_timeout(void* stream);
+
 /* --- log-mel front end -----------------------------------------------------
  * The showcase site, "The Solution" (mel_spectrogram.cu card: STFT, mel
  * filterbank, overlapping-chunk mode for long audio) and the PyPI page,

@@ -16,6 +16,7 @@ LIB_PATH = _build.LIB
 WB_OK, WB_EINVAL, WB_ECUDA, WB_EUNSUPPORTED, WB_ETIMEOUT, WB_EWORKSPACE = 0, -1, -2, -3, -4, -5
 WB_BF16, WB_E4M3 = 0, 1
 WB_LOGMEL_STATIC_MAX_CHUNKS = 2   # include/wb.h
+WB_SELFTEST_WAIT_SITE = 0x7F      # include/wb.h
 
 c_int, c_i64, c_size, c_void, c_float = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 P = ctypes.POINTER
@@ -53,6 +54,7 @@ SIGNATURES = {
     "wb_status_string": (ctypes.c_char_p, [c_int]),
     "wb_version": (c_int, []),
     "wb_check_device_error": (c_int, [c_void, P(ctypes.c_uint32)]),
+    "wb_selftest_wait_timeout": (c_int, [c_void]),
     "wb_logmel_workspace_bytes": (c_size, [c_int, c_int]),
     "wb_logmel": (c_int, [c_void, c_i64, c_i64, c_int, c_int, c_void, c_void, c_size, c_void]),
     "wb_logmel_static": (c_int, [c_void, c_i64, c_i64, c_int, c_int, c_void, c_void]),

@@ -12,7 +12,7 @@ import dataclasses
 import torch
 
 from . import _lib
-from ._lib import WB_BF16, WB_E4M3, call, load
+from ._lib import WB_BF16, WB_E4M3, WB_ETIMEOUT, WB_OK, WbError, call, load
 
 CHUNK_SAMPLES = 480000
 N_FRAMES = 3000
@@ -250,9 +250,21 @@ def profile_end() -> dict:
 
 
 def check_device_error(stream=None) -> int:
+    """Synchronize, read and clear the device error word; 0 when no kernel reported a fault.
+
+    A recorded timeout is returned as the raw word (bit 0 set, wait site in bits 8..15)
+    rather than raised; a failed synchronization raises WbError."""
     word = ctypes.c_uint32(0)
-    call("wb_check_device_error", _stream(stream), ctypes.byref(word))
+    st = load().wb_check_device_error(_stream(stream), ctypes.byref(word))
+    if st not in (WB_OK, WB_ETIMEOUT):
+        raise WbError("wb_check_device_error", st)
     return word.value
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait diagnostic: a wait that nothing satisfies gives up after ~2 s and
+    records a timeout at site WB_SELFTEST_WAIT_SITE (read it back with check_device_error)."""
+    call("wb_selftest_wait_timeout", _stream(stream))
 
 
 # --------------------------------- weights ------------------------------------

@@ -336,6 +336,13 @@ wb_status wb_check_device_error(void* stream, uint32_t* detail) {
   return (word & ERR_TIMEOUT) ? WB_ETIMEOUT : WB_OK;
 }
 
+wb_status wb_selftest_wait_timeout(void* stream) {
+  uint32_t* e = err_ptr();
+  if (!e) return WB_ECUDA;
+  WB_CUDA(launch_wait_timeout_selftest(e, WB_SELFTEST_WAIT_SITE, static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
 // ------------------------------- log-mel -----------------------------------
 size_t wb_logmel_workspace_bytes(int n_chunks, int n_mels) {
   (void)n_mels;

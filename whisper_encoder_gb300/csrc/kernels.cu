@@ -736,4 +736,23 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, 
   return cudaGetLastError();
 }
 
+// Diagnostic of the bounded-wait path: one thread waits on an mbarrier that
+// nothing ever arrives on.  mbar_wait gives up after its time limit, records
+// ERR_TIMEOUT with the site in the device error word and the kernel returns
+// normally, exactly as a stalled pipeline role would.
+__global__ void wait_timeout_selftest_kernel(uint32_t* err, uint32_t site) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0, err, &abort_flag, site);
+}
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint32_t site, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err, site);
+  return cudaGetLastError();
+}
+
 }  // namespace wb
