@@ -250,6 +250,23 @@ size_t wb_attention_workspace_bytes(int batch, int T, int n_heads);
 wb_status wb_attention(const void* q, const void* k, const void* v, int batch, int T, int n_heads, void* out,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* LayerNorm straight to FP8 E4M3 codes with one absmax scale per batch item
+ * (the pages' per-tensor-scaled E4M3 activations, one tensor per 30 s chunk):
+ * y = LN(x) as wb_layernorm computes it, rounded to bf16; amax[i] = max |y|
+ * over the rows of item i (rows i*rows_per_item .. (i+1)*rows_per_item - 1);
+ * q = E4M3_rn_satfinite(y * 448 / amax[i]) (scale 1 where amax[i] == 0), so
+ * y ~ q * amax[i] / 448.  The arithmetic of wb_layernorm followed by
+ * wb_quantize_fp8 of each item, without the bf16 round trip through memory
+ * (two passes over x: statistics + absmax, then codes); the row statistics
+ * are summed in another order, so a value lying on a rounding boundary can
+ * come out one bf16 / E4M3 step away from that two-call result.
+ * x: bf16 [rows, d]; g, b: float32 [d]; q: u8 [rows, d]; amax: float32
+ * [ceil(rows / rows_per_item)], overwritten; stats: float32 [rows][2] out,
+ * each row's (mean, rstd).  16-byte aligned (amax 4-byte); d a multiple of
+ * 128, <= 2048.  WB_EINVAL for bad sizes, pointers or alignment. */
+wb_status wb_layernorm_e4m3(const void* x, const float* g, const float* b, int rows, int d, float eps,
+                            int rows_per_item, uint8_t* q, float* amax, float* stats, void* stream);
+
 /* --- after the encoder: decoder cross-attention keys and values ---------------------
  * The showcase site, "The Solution" (decoder cross-attention is one of the three
  * attention patterns) and "The Approach" (decoder_cross_attn site): every decoder

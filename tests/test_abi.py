@@ -108,6 +108,12 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.wb_fold_layernorm(fake, None, None, fake, 16, 64, fake, fake, fake, None) == _lib.WB_EINVAL
     assert lib.wb_fold_layernorm(fake, None, fake, fake, 16, 64, odd, fake, fake, None) == _lib.WB_EINVAL
     assert lib.wb_fold_layernorm(None, None, None, None, 0, 64, None, None, None, None) == _lib.WB_OK
+    # LayerNorm to E4M3: no item size, bad width, missing statistics, misaligned codes, no rows
+    assert lib.wb_layernorm_e4m3(fake, fake, fake, 4, 256, 1e-5, 0, fake, fake, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_layernorm_e4m3(fake, fake, fake, 4, 200, 1e-5, 4, fake, fake, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_layernorm_e4m3(fake, fake, fake, 4, 256, 1e-5, 4, fake, fake, None, None) == _lib.WB_EINVAL
+    assert lib.wb_layernorm_e4m3(fake, fake, fake, 4, 256, 1e-5, 4, odd, fake, fake, None) == _lib.WB_EINVAL
+    assert lib.wb_layernorm_e4m3(None, None, None, 0, 256, 1e-5, 1, None, None, None, None) == _lib.WB_OK
 
 
 def _imports(path):

@@ -114,6 +114,40 @@ def test_layernorm_matches_oracle(wb, d, rows):
     assert rel_l2(to_np(y2), oenc.layer_norm(x.astype(np.float64), g, b)) < 4e-3
 
 
+@pytest.mark.parametrize("d,rows,rpi", [(1280, 3700, 1500), (384, 1500, 1500), (640, 301, 100), (128, 1, 1)])
+def test_layernorm_e4m3_matches_two_step_path_and_oracle(wb, d, rows, rpi):
+    rng = np.random.default_rng(d + rows)
+    x = rng.normal(0.3, 2.0, size=(rows, d)).astype(np.float32)
+    x[:, 5] *= 40.0                                    # an outlier feature, as in real activations
+    x = synthetic.round_to(x, "bf16")                  # the oracle sees exactly the bf16 input
+    g = (1 + 0.1 * rng.normal(size=d)).astype(np.float32)
+    b = (0.1 * rng.normal(size=d)).astype(np.float32)
+    q, amax, stats = wb.layernorm_e4m3(_bf16(x), _f32(g), _f32(b), 1e-5, rows_per_item=rpi)
+    assert wb.check_device_error() == 0
+    q, amax, stats = to_np(q).astype(np.uint8), to_np(amax), to_np(stats)
+    y = wb.layernorm(_bf16(x), _f32(g), _f32(b), 1e-5)           # bf16 LayerNorm, then a per-item quantiser
+    for i in range(0, rows, rpi):
+        yi = y[i:i + rpi]
+        qi, si = wb.quantize_fp8(yi)
+        # same arithmetic; the row statistics are summed in another order, so a value on a rounding
+        # boundary may land one bf16 / E4M3 step away
+        a2 = np.abs(to_np(yi)).max()
+        assert abs(amax[i // rpi] - a2) <= a2 * 2.0 ** -8
+        q2 = to_np(qi).astype(np.uint8)
+        diff = q[i:i + rpi] != q2
+        assert diff.mean() < 1e-4
+        assert np.all(np.abs(ofp8.e4m3_decode(q[i:i + rpi][diff]) - ofp8.e4m3_decode(q2[diff]))
+                      <= 2.0 ** -3 * np.abs(ofp8.e4m3_decode(q2[diff])) + 2.0 ** -9)
+        # against the float64 oracle: one E4M3 rounding (relative 2^-4) on top of bf16 LayerNorm accuracy
+        ref = oenc.layer_norm(x[i:i + rpi].astype(np.float64), g, b)
+        dec = ofp8.e4m3_decode(q[i:i + rpi]) * (amax[i // rpi] / 448.0)
+        assert np.all(np.abs(dec - ref) <= 0.07 * np.abs(ref) + amax[i // rpi] / 448.0 * 2.0 ** -8)
+    mu = x.astype(np.float64).mean(axis=1)
+    rs = 1.0 / np.sqrt(x.astype(np.float64).var(axis=1) + 1e-5)
+    np.testing.assert_allclose(stats[:, 0], mu, rtol=1e-4, atol=1e-4 * np.abs(x).max())
+    np.testing.assert_allclose(stats[:, 1], rs, rtol=1e-4)
+
+
 @pytest.mark.parametrize("B,T,H", [(1, 1500, 2), (2, 130, 3), (1, 64, 1), (1, 257, 2), (1, 1, 1), (1, 9, 1),
                                    (1, 127, 1), (1, 128, 2), (1, 129, 1), (2, 255, 1)])
 def test_attention_matches_oracle(wb, B, T, H):

@@ -70,6 +70,8 @@ SIGNATURES = {
     "wb_linear": (c_int, [c_void, c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void, c_int, c_void,
                           c_void, c_void]),
     "wb_layernorm": (c_int, [c_void, c_void, c_void, c_void, c_int, c_int, c_float, c_void, c_void, c_void]),
+    "wb_layernorm_e4m3": (c_int, [c_void, c_void, c_void, c_int, c_int, c_float, c_int, c_void, c_void, c_void,
+                                  c_void]),
     "wb_attention_workspace_bytes": (c_size, [c_int, c_int, c_int]),
     "wb_attention": (c_int, [c_void, c_void, c_void, c_int, c_int, c_int, c_void, c_void, c_size, c_void]),
     "wb_cross_kv": (c_int, [c_void, c_int, P(wb_dims), c_int, P(wb_cross_kv_weights), c_void, c_void]),

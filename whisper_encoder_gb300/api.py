@@ -183,6 +183,24 @@ def layernorm(x, g, b, eps: float = 1e-5, residual=None, return_total: bool = Fa
     return (y, total) if return_total else y
 
 
+def layernorm_e4m3(x, g, b, eps: float = 1e-5, rows_per_item: int | None = None, stream=None):
+    """LayerNorm to E4M3 codes with one absmax scale per item of rows_per_item rows (default: all rows).
+
+    Returns (codes u8 [rows, d], amax f32 [items], stats f32 [rows, 2] = (mean, rstd)); the
+    dequantised output is codes * amax[item] / 448."""
+    _need(x, torch.bfloat16, "x")
+    x2 = x.reshape(-1, x.shape[-1])
+    rows, d = x2.shape
+    rpi = rows if rows_per_item is None else int(rows_per_item)
+    items = (rows + rpi - 1) // rpi if rows else 0
+    q = torch.empty((rows, d), dtype=torch.uint8, device=x.device)
+    amax = torch.empty(max(items, 1), dtype=torch.float32, device=x.device)
+    stats = torch.empty((max(rows, 1), 2), dtype=torch.float32, device=x.device)
+    call("wb_layernorm_e4m3", _p(x2), _p(g), _p(b), rows, d, eps, max(rpi, 1), _p(q), _p(amax), _p(stats),
+         _stream(stream))
+    return q, amax[:items], stats[:rows]
+
+
 def attention(q, k, v, n_heads: int, stream=None) -> torch.Tensor:
     """q, k, v: bf16 [batch, T, 64*n_heads] -> softmax(q k^T / 8) v per head."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):

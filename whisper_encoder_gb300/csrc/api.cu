@@ -609,15 +609,13 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     const bool fq = fold_qkv(l), ff = fold_fc1(l);
     // LN1 -> a  [-> E4M3]  (folded: only the row statistics; QKV reads src itself)
     {
-      Prof pr(PC_ENC_LN, s);
+      Prof pr(PC_ENC_LN, s, !fq && q8 ? 2 : 1);
       if (fq)
         WB_CUDA(launch_ln_stats(src, M, D, eps, stats, s));
+      else if (q8)   // E4M3 operand: LayerNorm writes the codes itself
+        WB_CUDA(launch_layernorm_e4m3(src, W.ln1_g, W.ln1_b, M, D, eps, stats, am_qkv, T_TOK, aq, s));
       else
-        WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, q8 ? am_qkv : nullptr, T_TOK, s));
-    }
-    if (q8) {
-      Prof pr(PC_ENC_QUANT, s);
-      WB_CUDA(launch_quantize_rows(a, static_cast<long long>(M) * D, D, T_TOK, am_qkv, aq, s));
+        WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, nullptr, T_TOK, s));
     }
     {  // QKV projection: q | k to qk [M, 2D], v transposed to vt
       GemmParams p = base_params();
@@ -666,13 +664,12 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     if (ff) {
       Prof pr(PC_ENC_LN, s);
       WB_CUDA(launch_ln_stats(h, M, D, eps, stats, s));
+    } else if (f8) {
+      Prof pr(PC_ENC_LN, s, 2);
+      WB_CUDA(launch_layernorm_e4m3(h, W.ln2_g, W.ln2_b, M, D, eps, stats, am_fc1, T_TOK, aq, s));
     } else {
       Prof pr(PC_ENC_LN, s);
-      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, f8 ? am_fc1 : nullptr, T_TOK, s));
-    }
-    if (f8) {
-      Prof pr(PC_ENC_QUANT, s);
-      WB_CUDA(launch_quantize_rows(a, static_cast<long long>(M) * D, D, T_TOK, am_fc1, aq, s));
+      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, nullptr, T_TOK, s));
     }
     {  // FC1 + bias + GELU -> g
       GemmParams p = base_params();
@@ -789,6 +786,21 @@ wb_status wb_layernorm(const void* x, const void* residual, const float* g, cons
   WB_CUDA(launch_layernorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(residual), g, b,
                            rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total), nullptr, 0,
                            static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
+wb_status wb_layernorm_e4m3(const void* x, const float* g, const float* b, int rows, int d, float eps,
+                            int rows_per_item, uint8_t* q, float* amax, float* stats, void* stream) {
+  if (rows < 0 || d < 128 || d > 2048 || d % 128 != 0 || !(eps > 0.0f) || rows_per_item < 1) return WB_EINVAL;
+  if (rows == 0) return WB_OK;
+  if (!x || !g || !b || !q || !amax || !stats || !aligned16(x) || !aligned16(g) || !aligned16(b) || !aligned16(q) ||
+      !aligned16(stats) || (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return WB_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int items = (rows + rows_per_item - 1) / rows_per_item;
+  WB_CUDA(cudaMemsetAsync(amax, 0, sizeof(float) * items, s));
+  WB_CUDA(launch_layernorm_e4m3(static_cast<const __nv_bfloat16*>(x), g, b, rows, d, eps,
+                                reinterpret_cast<float2*>(stats), amax, rows_per_item, q, s));
   return WB_OK;
 }
 

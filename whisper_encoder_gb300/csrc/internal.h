@@ -34,6 +34,10 @@ cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, c
                              int rows_per_item, cudaStream_t s);
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
                            float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s);
+// LayerNorm to E4M3 codes in two passes (row statistics + per-item absmax, then codes); the same
+// widths as launch_layernorm (multiples of 128 up to 2048).
+cudaError_t launch_layernorm_e4m3(const __nv_bfloat16* x, const float* g, const float* b, int rows, int d, float eps,
+                                  float2* stats, float* amax, int rows_per_item, uint8_t* q, cudaStream_t s);
 cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s);
 cudaError_t launch_fold_ln(const __nv_bfloat16* w, const float* b, const float* gamma, const float* beta, int n_out,
                            int d, __nv_bfloat16* w_ln, float* c, float* b_ln, cudaStream_t s);

@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
       uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
       for (int j = 0; j < VEC / 2; ++j) {
-        const float y0 = (v[i * VEC + 2 * j] - mean) * rstd * gg[2 * j] + bb[2 * j];
-        const float y1 = (v[i * VEC + 2 * j + 1] - mean) * rstd * gg[2 * j + 1] + bb[2 * j + 1];
+        const float y0 = fmaf((v[i * VEC + 2 * j] - mean) * rstd, gg[2 * j], bb[2 * j]);
+        const float y1 = fmaf((v[i * VEC + 2 * j + 1] - mean) * rstd, gg[2 * j + 1], bb[2 * j + 1]);
         o32[j] = pack_bf16(y0, y1);
         if (amax) {
           const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&o32[j]);
@@ -294,6 +294,165 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) run_max = fmaxf(run_max, __shfl_xor_sync(0xffffffffu, run_max, o));
     if (lane == 0 && run_max > 0.0f) atomic_max_nonneg(amax + run_item, run_max);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// LayerNorm straight to E4M3 codes, in two passes over x (no bf16 output round trip).  The
+// per-item scale needs the absmax of the whole item's LayerNorm output before any code can be
+// written, so pass 1 computes the row statistics and that absmax (of the bf16-rounded output,
+// as the bf16 LayerNorm followed by the quantiser sees it) and pass 2 recomputes the output
+// from the statistics and writes code = E4M3_rn_satfinite(bf16(y) * 448 / amax[item]).
+// ---------------------------------------------------------------------------
+// Packed helpers for the E4M3 LayerNorm: y = fmaf((x - mean) * rstd, g, b) on pairs (lane-wise the
+// same IEEE operations as layernorm_kernel's output), then rounded to a bf16 pair.
+__device__ __forceinline__ uint64_t ln_affine_x2(uint64_t x2, uint64_t nmean2, uint64_t rstd2, uint64_t g2,
+                                                 uint64_t b2) {
+  const uint64_t one2 = f32x2_pack(1.0f, 1.0f);
+  return f32x2_fma(f32x2_mul(f32x2_fma(x2, one2, nmean2), rstd2), g2, b2);
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t v) {
+  float lo, hi;
+  f32x2_unpack(v, lo, hi);
+  return pack_bf16(lo, hi);
+}
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return f32x2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Pass 1: stats[row] = (mean, rstd) (two passes over the row held in registers, biased variance,
+// as layernorm_kernel), and amax[item] = max |bf16(LN(x; g, b))| over the rows of each item
+// (item = row / rows_per_item).  A warp per row, lane t owning columns 128k + 4t .. 4t+3, so that
+// the gamma / beta reads of a warp are contiguous; persistent, with the next row loaded while this
+// one is reduced.
+template <int NK>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+    ln_stats_amax_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ g,
+                         const float* __restrict__ bta, int rows, float eps, float2* __restrict__ stats,
+                         float* __restrict__ amax, int rows_per_item) {
+  constexpr int D = NK * 128;
+  const int lane = threadIdx.x & 31;
+  const long long warp_g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const long long per = (rows + n_warps - 1) / n_warps;
+  const long long r0 = warp_g * per;
+  const long long r1 = r0 + per < rows ? r0 + per : rows;
+  auto load = [&](long long row, uint2 (&u)[NK]) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) u[k] = __ldg(reinterpret_cast<const uint2*>(x + row * D + 128 * k) + lane);
+  };
+  uint2 u[NK], nu[NK];
+  if (r0 < r1) load(r0, u);
+  uint32_t run_max2 = 0u;                          // packed bf16 |y| maxima of the current item
+  int run_item = r0 < r1 ? static_cast<int>(r0 / rows_per_item) : 0;
+  auto flush = [&]() {
+    float m = fmaxf(__uint_as_float(run_max2 << 16), __uint_as_float(run_max2 & 0xffff0000u));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0 && m > 0.0f) atomic_max_nonneg(amax + run_item, m);
+  };
+  for (long long row = r0; row < r1; ++row) {
+    if (row + 1 < r1) load(row + 1, nu);
+    float sm = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NK; ++k)
+      sm += (__uint_as_float(u[k].x << 16) + __uint_as_float(u[k].x & 0xffff0000u)) +
+            (__uint_as_float(u[k].y << 16) + __uint_as_float(u[k].y & 0xffff0000u));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    const float mean = sm * (1.0f / D);
+    float q = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+      const float v[4] = {__uint_as_float(u[k].x << 16), __uint_as_float(u[k].x & 0xffff0000u),
+                          __uint_as_float(u[k].y << 16), __uint_as_float(u[k].y & 0xffff0000u)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) q = fmaf(v[j] - mean, v[j] - mean, q);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float rstd = rsqrtf(q * (1.0f / D) + eps);
+    if (lane == 0) stats[row] = make_float2(mean, rstd);
+    const int item = static_cast<int>(row / rows_per_item);
+    if (item != run_item) {                        // rows are contiguous per warp: items change rarely
+      flush();
+      run_max2 = 0u;
+      run_item = item;
+    }
+    const uint64_t nm2 = f32x2_pack(-mean, -mean), rs2 = f32x2_pack(rstd, rstd);
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+      const float4 g4 = __ldg(reinterpret_cast<const float4*>(g + 128 * k) + lane);
+      const float4 b4 = __ldg(reinterpret_cast<const float4*>(bta + 128 * k) + lane);
+      const uint32_t y01 = f32x2_to_bf16x2(
+          ln_affine_x2(bf16x2_to_f32x2(u[k].x), nm2, rs2, f32x2_pack(g4.x, g4.y), f32x2_pack(b4.x, b4.y)));
+      const uint32_t y23 = f32x2_to_bf16x2(
+          ln_affine_x2(bf16x2_to_f32x2(u[k].y), nm2, rs2, f32x2_pack(g4.z, g4.w), f32x2_pack(b4.z, b4.w)));
+      run_max2 = bf16x2_max(run_max2, bf16x2_max(y01 & 0x7fff7fffu, y23 & 0x7fff7fffu));
+    }
+#pragma unroll
+    for (int k = 0; k < NK; ++k) u[k] = nu[k];
+  }
+  if (r0 < r1) flush();
+}
+
+// Pass 2: q = E4M3 codes of bf16(LN(x)) scaled by 448 / amax[item] (1 if amax is 0), from the row
+// statistics.  Column-stationary: a block spans one row, thread t owning columns 8t .. 8t+7 (gamma and
+// beta in registers for every row it visits, one 16-byte load per row), and walks LNQ_ROWS consecutive
+// rows, LNQ_RG loads in flight per thread.
+constexpr int LNQ_RG = 8;
+constexpr int LNQ_ROWS = 32;
+__global__ void __launch_bounds__(256)
+    ln_quantize_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ g,
+                       const float* __restrict__ bta, const float2* __restrict__ stats, int rows, int d,
+                       const float* __restrict__ amax, int rows_per_item, uint8_t* __restrict__ q) {
+  const int t = threadIdx.x;
+  if (8 * t >= d) return;
+  const float4 ga = __ldg(reinterpret_cast<const float4*>(g) + 2 * t), gb = __ldg(reinterpret_cast<const float4*>(g) + 2 * t + 1);
+  const float4 ba = __ldg(reinterpret_cast<const float4*>(bta) + 2 * t), bb = __ldg(reinterpret_cast<const float4*>(bta) + 2 * t + 1);
+  const uint64_t g2[4] = {f32x2_pack(ga.x, ga.y), f32x2_pack(ga.z, ga.w), f32x2_pack(gb.x, gb.y), f32x2_pack(gb.z, gb.w)};
+  const uint64_t b2[4] = {f32x2_pack(ba.x, ba.y), f32x2_pack(ba.z, ba.w), f32x2_pack(bb.x, bb.y), f32x2_pack(bb.z, bb.w)};
+  const int row0 = blockIdx.x * LNQ_ROWS;
+  int item = row0 / rows_per_item;                 // items advance at most once every rows_per_item rows
+  int item_end = (item + 1) * rows_per_item;
+  float inv = 1.0f;
+  {
+    const float a = __ldg(amax + item);
+    inv = a > 0.0f ? 448.0f / a : 1.0f;
+  }
+  for (int rg = 0; rg < LNQ_ROWS; rg += LNQ_RG) {
+    const int rb = row0 + rg;
+    if (rb >= rows) break;
+    uint4 u[LNQ_RG];
+#pragma unroll
+    for (int r = 0; r < LNQ_RG; ++r)
+      u[r] = rb + r < rows ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(rb + r) * d) + t)
+                           : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int r = 0; r < LNQ_RG; ++r) {
+      const int row = rb + r;
+      if (row >= rows) break;
+      while (row >= item_end) {
+        ++item;
+        item_end += rows_per_item;
+        const float a = __ldg(amax + item);
+        inv = a > 0.0f ? 448.0f / a : 1.0f;
+      }
+      const float2 st = __ldg(stats + row);
+      const uint64_t nm2 = f32x2_pack(-st.x, -st.x), rs2 = f32x2_pack(st.y, st.y), inv2 = f32x2_pack(inv, inv);
+      const uint32_t w[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
+      uint32_t c[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float s0, s1, s2, s3;
+        f32x2_unpack(f32x2_mul(bf16x2_to_f32x2(f32x2_to_bf16x2(ln_affine_x2(bf16x2_to_f32x2(w[2 * k]), nm2, rs2,
+                                                                            g2[2 * k], b2[2 * k]))), inv2), s0, s1);
+        f32x2_unpack(f32x2_mul(bf16x2_to_f32x2(f32x2_to_bf16x2(ln_affine_x2(bf16x2_to_f32x2(w[2 * k + 1]), nm2, rs2,
+                                                                            g2[2 * k + 1], b2[2 * k + 1]))), inv2), s2, s3);
+        c[k] = static_cast<uint32_t>(cvt_e4m3x2(s0, s1)) | (static_cast<uint32_t>(cvt_e4m3x2(s2, s3)) << 16);
+      }
+      reinterpret_cast<uint2*>(q + static_cast<long long>(row) * d)[t] = make_uint2(c[0], c[1]);
+    }
   }
 }
 
@@ -650,6 +809,48 @@ static cudaError_t norm_dispatch(const __nv_bfloat16* x, const __nv_bfloat16* re
       return cudaErrorInvalidValue;
   }
 #undef WB_LN_CASE
+}
+
+template <int NK>
+static cudaError_t ln_e4m3_launch(const __nv_bfloat16* x, const float* g, const float* b, int rows, float eps,
+                                  float2* stats, float* amax, int rows_per_item, uint8_t* q, cudaStream_t s) {
+  constexpr int D = NK * 128;
+  long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
+  const long long cap = 2LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  ln_stats_amax_kernel<NK><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(x, g, b, rows, eps, stats, amax,
+                                                                            rows_per_item);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int threads = ((D / 8 + 31) / 32) * 32;
+  ln_quantize_kernel<<<(rows + LNQ_ROWS - 1) / LNQ_ROWS, threads, 0, s>>>(x, g, b, stats, rows, D, amax, rows_per_item,
+                                                                         q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm_e4m3(const __nv_bfloat16* x, const float* g, const float* b, int rows, int d, float eps,
+                                  float2* stats, float* amax, int rows_per_item, uint8_t* q, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int rpi = rows_per_item > 0 ? rows_per_item : rows;
+  switch (d) {
+    case 128: return ln_e4m3_launch<1>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 256: return ln_e4m3_launch<2>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 384: return ln_e4m3_launch<3>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 512: return ln_e4m3_launch<4>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 640: return ln_e4m3_launch<5>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 768: return ln_e4m3_launch<6>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 896: return ln_e4m3_launch<7>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1024: return ln_e4m3_launch<8>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1152: return ln_e4m3_launch<9>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1280: return ln_e4m3_launch<10>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1408: return ln_e4m3_launch<11>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1536: return ln_e4m3_launch<12>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1664: return ln_e4m3_launch<13>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1792: return ln_e4m3_launch<14>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 1920: return ln_e4m3_launch<15>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    case 2048: return ln_e4m3_launch<16>(x, g, b, rows, eps, stats, amax, rpi, q, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,

@@ -393,6 +393,56 @@ __device__ __forceinline__ float gelu_fast(float x) {
   return x * (x >= 0.0f ? 1.0f - half_erfc : half_erfc);
 }
 
+// Packed fp32 pairs (one 64-bit register pair, lane-wise IEEE arithmetic).
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {   // a * b + c
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// gelu_fast on a pair of values with packed fp32 arithmetic: the same Abramowitz & Stegun 7.1.26
+// evaluation (t = 1 / (1 + p |x| / sqrt 2), erfc(|x| / sqrt 2) / 2 = t poly(t) 2^(-x^2 log2(e) / 2 - 1)),
+// with |x| / sqrt 2 folded into the constant p / sqrt 2 and z^2 written as x^2 / 2.
+__device__ __forceinline__ void gelu_fast_x2(float& x0, float& x1) {
+  const uint64_t x = f32x2_pack(x0, x1);
+  const uint64_t ax = x & 0x7fffffff7fffffffull;
+  const uint64_t den = f32x2_fma(ax, f32x2_pack(0.23164190f, 0.23164190f), f32x2_pack(1.0f, 1.0f));
+  float d0, d1;
+  f32x2_unpack(den, d0, d1);
+  const uint64_t t = f32x2_pack(rcp_approx(d0), rcp_approx(d1));
+  uint64_t q = f32x2_fma(t, f32x2_pack(1.061405429f, 1.061405429f), f32x2_pack(-1.453152027f, -1.453152027f));
+  q = f32x2_fma(t, q, f32x2_pack(1.421413741f, 1.421413741f));
+  q = f32x2_fma(t, q, f32x2_pack(-0.284496736f, -0.284496736f));
+  q = f32x2_fma(t, q, f32x2_pack(0.254829592f, 0.254829592f));
+  q = f32x2_mul(q, t);
+  const uint64_t ea = f32x2_fma(f32x2_mul(x, x), f32x2_pack(-0.72134752044448170f, -0.72134752044448170f),
+                                f32x2_pack(-1.0f, -1.0f));
+  float e0, e1;
+  f32x2_unpack(ea, e0, e1);
+  const uint64_t xh = f32x2_mul(x, f32x2_mul(q, f32x2_pack(ex2_approx(e0), ex2_approx(e1))));   // x erfc / 2
+  const uint64_t dm = f32x2_fma(xh, f32x2_pack(-1.0f, -1.0f), x);                                  // x - x erfc / 2
+  float h0, h1, m0, m1;
+  f32x2_unpack(xh, h0, h1);
+  f32x2_unpack(dm, m0, m1);
+  x0 = x0 >= 0.0f ? m0 : h0;
+  x1 = x1 >= 0.0f ? m1 : h1;
+}
+
+// Packed bf16x2 maximum.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
