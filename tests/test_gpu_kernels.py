@@ -172,6 +172,22 @@ def test_attention_peaked_scores(wb):
     assert rel_l2(out[0], oenc.attention(q[0].astype(np.float64), k[0], v[0], H)) < 1e-2
 
 
+@pytest.mark.parametrize("growth", [3.0, 12.0])
+def test_attention_maxima_growing_along_the_keys(wb, growth):
+    # scores rise steadily along the sequence, so the running row maxima move at some (growth 3) or
+    # every (growth 12) later key tile: the paths that move the maxima and rescale O after tile 0
+    rng = np.random.default_rng(int(growth))
+    B, T, H = 1, 1500, 2
+    base = rng.normal(size=(1, 1, 64 * H))
+    q = synthetic.round_to((base + 0.1 * rng.normal(size=(B, T, 64 * H))).astype(np.float32), "bf16")
+    ramp = (growth * np.arange(T) / T)[None, :, None]
+    k = synthetic.round_to((base * ramp + 0.3 * rng.normal(size=(B, T, 64 * H))).astype(np.float32), "bf16")
+    v = synthetic.round_to(rng.normal(size=(B, T, 64 * H)).astype(np.float32), "bf16")
+    out = to_np(wb.attention(_bf16(q), _bf16(k), _bf16(v), H))
+    assert wb.check_device_error() == 0
+    assert rel_l2(out[0], oenc.attention(q[0].astype(np.float64), k[0], v[0], H)) < 1e-2
+
+
 def test_attention_single_key_returns_v(wb):
     # T = 1: the only weight is 1 and the row sum is 1, so every output equals v (bf16 -> f16 -> bf16 is exact)
     rng = np.random.default_rng(5)

@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
           if (col + 1 >= valid) s[4 * kk + 1] = s[4 * kk + 3] = -INFINITY;
         }
       }
+      // this thread's share (32 scores) of the maxima of rows ra and ra + 8
       float xa0 = fmaxf(s[0], s[1]), xa1 = fmaxf(s[4], s[5]);
       float xb0 = fmaxf(s[2], s[3]), xb1 = fmaxf(s[6], s[7]);
 #pragma unroll
@@ -234,28 +235,33 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
         xb1 = fmax3(xb1, s[4 * kk + 6], s[4 * kk + 7]);
       }
       float xa = fmaxf(xa0, xa1), xb = fmaxf(xb0, xb1);
-      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
-      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
-      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
-      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
-      const float ca = xa * c, cb = xb * c;
       float alpha_a = 1.0f, alpha_b = 1.0f;
       bool rescale = false;
-      if (j == 0) {
-        m_a = ca;
-        m_b = cb;
-      } else {
-        if (ca > m_a + RESCALE_LOG2) {
-          alpha_a = ex2_approx(m_a - ca);
+      // From the second key tile on, the running maxima only move where a row's new maximum passes
+      // them by more than 2^8; a vote on the threads' partial maxima finds the (rare) tiles where that
+      // can happen, and only those pay for combining the row maxima across the four threads of a row.
+      if (j == 0 || __any_sync(0xffffffffu, xa * c > m_a + RESCALE_LOG2 || xb * c > m_b + RESCALE_LOG2)) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
+        const float ca = xa * c, cb = xb * c;
+        if (j == 0) {
           m_a = ca;
-          l_a *= alpha_a;
-          rescale = true;
-        }
-        if (cb > m_b + RESCALE_LOG2) {
-          alpha_b = ex2_approx(m_b - cb);
           m_b = cb;
-          l_b *= alpha_b;
-          rescale = true;
+        } else {
+          if (ca > m_a + RESCALE_LOG2) {
+            alpha_a = ex2_approx(m_a - ca);
+            m_a = ca;
+            l_a *= alpha_a;
+            rescale = true;
+          }
+          if (cb > m_b + RESCALE_LOG2) {
+            alpha_b = ex2_approx(m_b - cb);
+            m_b = cb;
+            l_b *= alpha_b;
+            rescale = true;
+          }
         }
       }
       // pw[2k]: row ra, P column 4k + t % 4 (keys 8k + cq, + 1); pw[2k+1]: row ra + 8, same column

@@ -325,7 +325,7 @@ __device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
 // (item = row / rows_per_item).  A warp per row, lane t owning columns 128k + 4t .. 4t+3, so that
 // the gamma / beta reads of a warp are contiguous; persistent, with the next row loaded while this
 // one is reduced.
-template <int NK>
+template <int NK, bool AMAX>
 __global__ void __launch_bounds__(LN_WARPS * 32)
     ln_stats_amax_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ g,
                          const float* __restrict__ bta, int rows, float eps, float2* __restrict__ stats,
@@ -373,6 +373,11 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
     for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
     const float rstd = rsqrtf(q * (1.0f / D) + eps);
     if (lane == 0) stats[row] = make_float2(mean, rstd);
+    if (!AMAX) {
+#pragma unroll
+      for (int k = 0; k < NK; ++k) u[k] = nu[k];
+      continue;
+    }
     const int item = static_cast<int>(row / rows_per_item);
     if (item != run_item) {                        // rows are contiguous per warp: items change rarely
       flush();
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 #pragma unroll
     for (int k = 0; k < NK; ++k) u[k] = nu[k];
   }
-  if (r0 < r1) flush();
+  if (AMAX && r0 < r1) flush();
 }
 
 // Pass 2: q = E4M3 codes of bf16(LN(x)) scaled by 448 / amax[item] (1 if amax is 0), from the row
@@ -818,8 +823,8 @@ static cudaError_t ln_e4m3_launch(const __nv_bfloat16* x, const float* g, const 
   long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
   const long long cap = 2LL * sm_count();
   if (blocks > cap) blocks = cap;
-  ln_stats_amax_kernel<NK><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(x, g, b, rows, eps, stats, amax,
-                                                                            rows_per_item);
+  ln_stats_amax_kernel<NK, true><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(x, g, b, rows, eps, stats, amax,
+                                                                                  rows_per_item);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int threads = ((D / 8 + 31) / 32) * 32;
@@ -864,7 +869,29 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, con
   return norm_dispatch<true>(x, res, g, nullptr, rows, d, eps, y, total, nullptr, 0, s);
 }
 
+template <int NK>
+static cudaError_t ln_stats_launch(const __nv_bfloat16* x, int rows, float eps, float2* out, cudaStream_t s) {
+  long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
+  const long long cap = 2LL * sm_count();
+  if (blocks > cap) blocks = cap;
+  ln_stats_amax_kernel<NK, false><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(x, nullptr, nullptr, rows, eps, out,
+                                                                                   nullptr, 1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s) {
+  // widths that are multiples of 128 (every Whisper size): the persistent row walk
+  if (rows > 0 && rows < (1LL << 31)) {
+    const int r = static_cast<int>(rows);
+    switch (d) {
+      case 384: return ln_stats_launch<3>(x, r, eps, out, s);
+      case 512: return ln_stats_launch<4>(x, r, eps, out, s);
+      case 768: return ln_stats_launch<6>(x, r, eps, out, s);
+      case 1024: return ln_stats_launch<8>(x, r, eps, out, s);
+      case 1280: return ln_stats_launch<10>(x, r, eps, out, s);
+      default: break;
+    }
+  }
   if (d <= 0 || d % 8 || d > STATS_MAXC * 32 * 8) return cudaErrorInvalidValue;
   if (rows == 0) return cudaSuccess;
   const long long blocks = (rows + 7) / 8;               // 8 warps per block, a warp per row
