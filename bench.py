@@ -89,7 +89,7 @@ def step_roofline(fl: dict, by: dict, B: int, peaks: dict, fp8_classes: set, ms_
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture of the
 # kernel class at the batch-32 shape (profiles/); None where the code changed since the capture.
-TRAFFIC = {"enc.attention": 474.0e6}
+TRAFFIC = {"enc.attention": 473.5e6}
 
 
 def load_peaks() -> dict:
@@ -275,6 +275,13 @@ def run_case(args) -> None:
         bet = torch.zeros(d, device="cuda")
         fn = lambda: wb.layernorm(x, gam, bet)  # noqa: E731
         flops = 2.0 * M * d * 2      # bytes moved (read + write), reported in the same field
+    elif args.case == "layernorm_e4m3":
+        # LayerNorm straight to E4M3 codes with one scale per 1500-row chunk (the mixed_fp8 LN1 / LN2 sites)
+        x = rnd(M, d, scale=2.0)
+        gam = torch.ones(d, device="cuda")
+        bet = torch.zeros(d, device="cuda")
+        fn = lambda: wb.layernorm_e4m3(x, gam, bet, rows_per_item=1500)  # noqa: E731
+        flops = M * d * 2.0 + M * d      # bytes: bf16 rows read, E4M3 codes written
     elif args.case == "longform":
         # 45 min of synthetic audio in 30 s windows at a 25 s stride (the PyPI page's overlapping-chunk
         # mode): 108 windows through the same three calls in 3 batches of 36, audio already on the device
@@ -317,8 +324,9 @@ def run_case(args) -> None:
     torch.cuda.synchronize()
     ms = ev[0].elapsed_time(ev[1]) / 3
     rate = flops / (ms / 1000)
+    hbm = args.case.startswith("layernorm")
     print(json.dumps({"case": args.case, "batch": B, "ms": round(ms, 4),
-                      ("gbs" if args.case == "layernorm" else "tflops"): round(rate / (1e9 if args.case == "layernorm" else 1e12), 1)}))
+                      ("gbs" if hbm else "tflops"): round(rate / (1e9 if hbm else 1e12), 1)}))
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -332,7 +340,8 @@ def main() -> None:
     ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph of the three calls")
-    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "logmel", "longform"),
+    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "layernorm_e4m3", "logmel",
+                                       "longform"),
                     default=None,
                     help="launch one kernel class at full size (for profiler captures) instead of the bench")
     args = ap.parse_args()
