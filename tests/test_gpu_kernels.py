@@ -38,6 +38,19 @@ def test_linear_bf16_small_integers_bit_exact(wb, M, N, K):
     np.testing.assert_array_equal(to_np(out), ref.astype(np.float64))
 
 
+@pytest.mark.parametrize("M,N,K", [(25600, 1152, 64), (48000, 1280, 128)])
+def test_linear_bf16_wide_tiles_bit_exact(wb, M, N, K):
+    # M large enough that the 256-column tiles are chosen (ragged last column tile for N = 1152); the
+    # small-M cases above run 128-column tiles
+    a, w = synthetic.gemm_operands(M + N, M, N, K, -1, 1)
+    rng = np.random.default_rng(N)
+    bias = rng.integers(-4, 5, N).astype(np.float32)
+    ref = a.astype(np.float64) @ w.astype(np.float64).T + bias      # small integers: exact in float64
+    out = wb.linear(_bf16(a), _bf16(w), bias=_f32(bias), gelu=False)
+    assert wb.check_device_error() == 0
+    np.testing.assert_array_equal(to_np(out), ref)
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 256, 256), (257, 1280, 640)])
 def test_linear_e4m3_small_integers_bit_exact(wb, M, N, K):
     a, w = synthetic.gemm_operands(5 * M + K, M, N, K, -2, 2)
