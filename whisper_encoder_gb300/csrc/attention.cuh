@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // barriers and TMEM are set up: from here on the kernel reads its inputs
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   if (warp == 0) {
     if (lane == 0) {

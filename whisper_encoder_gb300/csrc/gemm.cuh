@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // barriers and TMEM are set up: from here on the kernel reads its inputs
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   const int m_tiles = (p.M + GEMM_BM - 1) / GEMM_BM;
   const int n_tiles = (p.N + BN - 1) / BN;

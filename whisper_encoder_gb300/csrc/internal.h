@@ -61,6 +61,24 @@ cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long
                              int batch, int row, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint32_t site, cudaStream_t s);
 
+// Launch with programmatic stream serialization: the kernel may begin (its prologue, up to its
+// grid_dependency_wait()) while the previous kernel in the stream is still finishing.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---- tensor-core kernels (tc_kernels.cu) ----
 struct GemmLaunch {
   CUtensorMap amap[GEMM_MAX_AMAPS];

@@ -331,6 +331,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
                          const float* __restrict__ bta, int rows, float eps, float2* __restrict__ stats,
                          float* __restrict__ amax, int rows_per_item) {
   constexpr int D = NK * 128;
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int lane = threadIdx.x & 31;
   const long long warp_g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -411,6 +413,8 @@ __global__ void __launch_bounds__(256)
     ln_quantize_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ g,
                        const float* __restrict__ bta, const float2* __restrict__ stats, int rows, int d,
                        const float* __restrict__ amax, int rows_per_item, uint8_t* __restrict__ q) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int t = threadIdx.x;
   if (8 * t >= d) return;
   const float4 ga = __ldg(reinterpret_cast<const float4*>(g) + 2 * t), gb = __ldg(reinterpret_cast<const float4*>(g) + 2 * t + 1);
@@ -823,14 +827,12 @@ static cudaError_t ln_e4m3_launch(const __nv_bfloat16* x, const float* g, const 
   long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
   const long long cap = 2LL * sm_count();
   if (blocks > cap) blocks = cap;
-  ln_stats_amax_kernel<NK, true><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(x, g, b, rows, eps, stats, amax,
-                                                                                  rows_per_item);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(ln_stats_amax_kernel<NK, true>, dim3(static_cast<unsigned>(blocks)), dim3(LN_WARPS * 32), 0,
+                             s, x, g, b, rows, eps, stats, amax, rows_per_item);
   if (e != cudaSuccess) return e;
   const int threads = ((D / 8 + 31) / 32) * 32;
-  ln_quantize_kernel<<<(rows + LNQ_ROWS - 1) / LNQ_ROWS, threads, 0, s>>>(x, g, b, stats, rows, D, amax, rows_per_item,
-                                                                         q);
-  return cudaGetLastError();
+  return launch_pdl(ln_quantize_kernel, dim3((rows + LNQ_ROWS - 1) / LNQ_ROWS), dim3(threads), 0, s, x, g, b,
+                    static_cast<const float2*>(stats), rows, D, static_cast<const float*>(amax), rows_per_item, q);
 }
 
 cudaError_t launch_layernorm_e4m3(const __nv_bfloat16* x, const float* g, const float* b, int rows, int d, float eps,
@@ -874,9 +876,9 @@ static cudaError_t ln_stats_launch(const __nv_bfloat16* x, int rows, float eps, 
   long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
   const long long cap = 2LL * sm_count();
   if (blocks > cap) blocks = cap;
-  ln_stats_amax_kernel<NK, false><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(x, nullptr, nullptr, rows, eps, out,
-                                                                                   nullptr, 1);
-  return cudaGetLastError();
+  return launch_pdl(ln_stats_amax_kernel<NK, false>, dim3(static_cast<unsigned>(blocks)), dim3(LN_WARPS * 32), 0, s, x,
+                    static_cast<const float*>(nullptr), static_cast<const float*>(nullptr), rows, eps, out,
+                    static_cast<float*>(nullptr), 1);
 }
 
 cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s) {

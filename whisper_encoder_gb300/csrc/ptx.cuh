@@ -34,6 +34,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 
+// ------------------------ programmatic dependent launch ------------------------
+// Kernels launched with the programmatic-serialization attribute may start while the previous
+// kernel in the stream is finishing.  grid_dependency_wait() returns once the grids this one depends
+// on have completed and their writes are visible: every read of a predecessor's output, and every
+// write, comes after it.  grid_dependents_launch() lets the next such kernel begin launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------- mbarrier ------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

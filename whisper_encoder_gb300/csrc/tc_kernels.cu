@@ -58,8 +58,8 @@ cudaError_t gemm_launch_t(const GemmLaunch& g, cudaStream_t s) {
   int grid = sm_count();
   if (tiles < grid) grid = static_cast<int>(tiles);
   if (grid < 1) return cudaSuccess;
-  kern<<<grid, GEMM_THREADS, smem, s>>>(g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap, g.omap, g.p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(GEMM_THREADS), smem, s, g.amap[0], g.amap[1], g.amap[2], g.amap[3], g.bmap,
+                    g.omap, g.p);
 }
 
 }  // namespace
@@ -97,8 +97,7 @@ cudaError_t launch_attention(const CUtensorMap& q, const CUtensorMap& k, const C
   const int n_qt = (p.T + ATT_BQ - 1) / ATT_BQ;
   const long long grid = static_cast<long long>(p.batch) * p.H * n_qt;
   if (grid < 1) return cudaSuccess;
-  attention_kernel<<<static_cast<unsigned>(grid), ATT_THREADS, smem, s>>>(q, k, vt, p);
-  return cudaGetLastError();
+  return launch_pdl(attention_kernel, dim3(static_cast<unsigned>(grid)), dim3(ATT_THREADS), smem, s, q, k, vt, p);
 }
 
 }  // namespace wb
