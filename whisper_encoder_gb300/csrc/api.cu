@@ -181,20 +181,24 @@ void one_pass(GemmParams& p, int n_kb) {
 
 // Plain GEMM out[M, N] = epilogue(A[M, K] . W[N, K]^T), A and W dense row-major; the output
 // (and residual) rows are ldo elements apart, and the output map covers its first n_store columns.
+// Tile width for an M x N output (per batch item, `items` items).  Wide N takes 256-column tiles; when M
+// is small (a few chunks) 128-wide tiles are used if the waves they need, at about 0.7 of a 256-wide
+// tile's time each (half the work, a less efficient MMA shape; measured 0.65-0.74 at N = 1280), finish
+// sooner than the 256-wide waves.
+int pick_bn(long long M, long long items, int N) {
+  if (!(N % 256 == 0 || N > 512)) return 128;
+  const long long sms = sm_count(), mt = items * ((M + GEMM_BM - 1) / GEMM_BM);
+  const long long w256 = (mt * ((N + 255) / 256) + sms - 1) / sms;
+  const long long w128 = (mt * ((N + 127) / 128) + sms - 1) / sms;
+  return 7 * w128 < 10 * w256 ? 128 : 256;
+}
+
 wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8, int epi, void* out, long long ldo,
                      int n_store, const void* resid, GemmParams p, cudaStream_t s, int prof_cls = PC_OTHER) {
   GemmLaunch g;
   std::memset(&g, 0, sizeof(g));
   const uint64_t es = fp8 ? 1 : 2;
-  g.bn = (N % 256 == 0 || N > 512) ? 256 : 128;
-  if (g.bn == 256) {
-    // Small M (a few chunks): 128-wide tiles when the waves they need, at about 0.6 of a 256-wide tile's
-    // time each (half the work, a less efficient MMA shape), finish sooner than the 256-wide waves.
-    const long long sms = sm_count(), mt = (M + GEMM_BM - 1) / GEMM_BM;
-    const long long w256 = (mt * ((N + 255) / 256) + sms - 1) / sms;
-    const long long w128 = (mt * ((N + 127) / 128) + sms - 1) / sms;
-    if (w128 * 3 < w256 * 5) g.bn = 128;
-  }
+  g.bn = pick_bn(M, 1, N);
   g.fp8 = fp8;
   g.epi = epi;
   if (!a_map(&g.amap[0], fp8, A, K, M, 1, 1, K * es, static_cast<uint64_t>(M) * K * es,
@@ -478,7 +482,6 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
   auto* yTp = reinterpret_cast<__nv_bfloat16*>(ws + L.yTp);
   auto* y1p = reinterpret_cast<__nv_bfloat16*>(ws + L.y1p);
   const int C = dims->n_mels, D = dims->d_model;
-  const int bn = (D % 256 == 0) ? 256 : 128;
 
   {
     Prof pr(PC_STEM_PREP, s, 4);
@@ -488,6 +491,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
   {  // conv1: three taps = three passes over row-shifted views of yTp
     GemmLaunch g;
     std::memset(&g, 0, sizeof(g));
+    const int bn = D % 256 == 0 ? pick_bn(N_FRAMES, batch, D) : 128;
     g.bn = bn;
     g.epi = EPI_BIAS_GELU;
     const uint64_t rs = static_cast<uint64_t>(C) * 2, item = static_cast<uint64_t>(N_FRAMES + 2) * C * 2;
@@ -513,6 +517,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
   {  // conv2: stride 2 -> one tensor map per tap over every other row of y1p
     GemmLaunch g;
     std::memset(&g, 0, sizeof(g));
+    const int bn = D % 256 == 0 ? pick_bn(T_TOK, batch, D) : 128;
     g.bn = bn;
     g.epi = EPI_CONV2;
     const uint64_t rs = static_cast<uint64_t>(2 * D) * 2;

@@ -50,36 +50,36 @@ __global__ void pad_split_kernel(const float* __restrict__ audio, long long n_sa
 // Windowed real-DFT basis, [3 parts][512 rows][400]: rows 256*t + c hold, for
 // tile t, c < 128: w[k] cos(2 pi bin k / 400) and c >= 128: -w[k] sin(...),
 // bin = 128 t + (c mod 128); bins above 200 are zero.  The phase index
-// bin*k mod 400 is reduced exactly in integers; values are formed in double
-// and split into three bf16 parts.
+// bin*k mod 400 is reduced exactly in integers; values are formed in float (the
+// three bf16 parts that follow carry 24 bits, a float's precision) and split.
 __global__ void dft_basis_kernel(__nv_bfloat16* __restrict__ basis) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= DFT_ROWS * N_FFT) return;
   const int row = idx / N_FFT, k = idx % N_FFT;
   const int tile = row / 256, col = row % 256;
   const int bin = tile * 128 + (col & 127);
-  double v = 0.0;
+  float v = 0.0f;
   if (bin <= N_FFT / 2) {
-    const double w = 0.5 - 0.5 * cospi(static_cast<double>(k) / 200.0);
+    const float w = 0.5f - 0.5f * cospif(static_cast<float>(k) / 200.0f);
     const int ph = (bin * k) % N_FFT;
-    double s, c;
-    sincospi(static_cast<double>(ph) / 200.0, &s, &c);
+    float s, c;
+    sincospif(static_cast<float>(ph) / 200.0f, &s, &c);
     v = w * (col >= 128 ? -s : c);
   }
-  const __nv_bfloat16 a = __double2bfloat16(v);
-  const double r1 = v - static_cast<double>(__bfloat162float(a));
-  const __nv_bfloat16 b = __double2bfloat16(r1);
-  const __nv_bfloat16 e = __double2bfloat16(r1 - static_cast<double>(__bfloat162float(b)));
+  const __nv_bfloat16 a = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(a);
+  const __nv_bfloat16 b = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 e = __float2bfloat16_rn(r1 - __bfloat162float(b));
   basis[(0 * DFT_ROWS + row) * N_FFT + k] = a;
   basis[(1 * DFT_ROWS + row) * N_FFT + k] = b;
   basis[(2 * DFT_ROWS + row) * N_FFT + k] = e;
 }
 
-__device__ double hz_to_mel(double f) {
-  return f < 1000.0 ? 3.0 * f / 200.0 : 15.0 + 27.0 * log(f / 1000.0) / log(6.4);
+__device__ float hz_to_mel(float f) {
+  return f < 1000.0f ? 3.0f * f / 200.0f : 15.0f + 27.0f * logf(f / 1000.0f) / logf(6.4f);
 }
-__device__ double mel_to_hz(double m) {
-  return m < 15.0 ? 200.0 * m / 3.0 : 1000.0 * exp((m - 15.0) * log(6.4) / 27.0);
+__device__ float mel_to_hz(float m) {
+  return m < 15.0f ? 200.0f * m / 3.0f : 1000.0f * expf((m - 15.0f) * logf(6.4f) / 27.0f);
 }
 
 // Slaney mel filterbank over 0-8 kHz at the 201 bins of a 400-point DFT,
@@ -90,16 +90,16 @@ __global__ void mel_fb_kernel(__nv_bfloat16* __restrict__ fbs, int n_mels) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= MEL_ROWS * N_BIN_PAD) return;
   const int m = idx / N_BIN_PAD, k = idx % N_BIN_PAD;
-  double v = 0.0;
+  float v = 0.0f;
   if (m < n_mels && k <= N_FFT / 2) {
-    const double step = hz_to_mel(8000.0) / (n_mels + 1);
-    const double lo = mel_to_hz(m * step), ce = mel_to_hz((m + 1) * step), hi = mel_to_hz((m + 2) * step);
-    const double f = 40.0 * k;
-    const double up = (f - lo) / (ce - lo), dn = (hi - f) / (hi - ce);
-    v = fmax(0.0, fmin(up, dn)) * 2.0 / (hi - lo);
+    const float step = hz_to_mel(8000.0f) / static_cast<float>(n_mels + 1);
+    const float lo = mel_to_hz(m * step), ce = mel_to_hz((m + 1) * step), hi = mel_to_hz((m + 2) * step);
+    const float f = 40.0f * k;
+    const float up = (f - lo) / (ce - lo), dn = (hi - f) / (hi - ce);
+    v = fmaxf(0.0f, fminf(up, dn)) * 2.0f / (hi - lo);
   }
-  const __nv_bfloat16 a = __double2bfloat16(v);
-  const __nv_bfloat16 b = __double2bfloat16(v - static_cast<double>(__bfloat162float(a)));
+  const __nv_bfloat16 a = __float2bfloat16_rn(v);
+  const __nv_bfloat16 b = __float2bfloat16_rn(v - __bfloat162float(a));
   fbs[m * N_BIN_PAD + k] = a;
   fbs[(MEL_ROWS + m) * N_BIN_PAD + k] = b;
 }
