@@ -628,7 +628,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
       else if (q8)   // E4M3 operand: LayerNorm writes the codes itself
         WB_CUDA(launch_layernorm_e4m3(src, W.ln1_g, W.ln1_b, M, D, eps, stats, am_qkv, T_TOK, aq, s));
       else
-        WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, nullptr, T_TOK, s));
+        WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, s));
     }
     {  // QKV projection: q | k to qk [M, 2D], v transposed to vt
       GemmParams p = base_params();
@@ -682,7 +682,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
       WB_CUDA(launch_layernorm_e4m3(h, W.ln2_g, W.ln2_b, M, D, eps, stats, am_fc1, T_TOK, aq, s));
     } else {
       Prof pr(PC_ENC_LN, s);
-      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, nullptr, T_TOK, s));
+      WB_CUDA(launch_layernorm(h, nullptr, W.ln2_g, W.ln2_b, M, D, eps, a, nullptr, s));
     }
     {  // FC1 + bias + GELU -> g
       GemmParams p = base_params();
@@ -724,7 +724,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
   const __nv_bfloat16* final_src = n_layers_run > 0 ? h : x0b;
   if (apply_final_ln) {
     Prof pr(PC_ENC_LN, s);
-    WB_CUDA(launch_layernorm(final_src, nullptr, ln_post->g, ln_post->b, M, D, eps, outb, nullptr, nullptr, 0, s));
+    WB_CUDA(launch_layernorm(final_src, nullptr, ln_post->g, ln_post->b, M, D, eps, outb, nullptr, s));
   } else if (n_layers_run == 0) {
     WB_CUDA(cudaMemcpyAsync(outb, x0b, static_cast<size_t>(M) * D * 2, cudaMemcpyDeviceToDevice, s));
   }
@@ -797,7 +797,7 @@ wb_status wb_layernorm(const void* x, const void* residual, const float* g, cons
   if (!x || !g || !b || !y || !aligned16(x) || !aligned16(y) || !aligned16(g) || !aligned16(b)) return WB_EINVAL;
   if ((residual && !aligned16(residual)) || (total && (!residual || !aligned16(total)))) return WB_EINVAL;
   WB_CUDA(launch_layernorm(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(residual), g, b,
-                           rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total), nullptr, 0,
+                           rows, d, eps, static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(total),
                            static_cast<cudaStream_t>(stream)));
   return WB_OK;
 }

@@ -30,8 +30,7 @@ cudaError_t launch_stem_transpose(const float* logmel, int batch, int n_mels, __
                                   cudaStream_t s);
 cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16* packed, cudaStream_t s);
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
-                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             int rows_per_item, cudaStream_t s);
+                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s);
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
                            float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s);
 // LayerNorm to E4M3 codes in two passes (row statistics + per-item absmax, then codes); the same

@@ -187,14 +187,12 @@ __device__ __forceinline__ void ln_load(const __nv_bfloat16* __restrict__ x, con
 }
 
 // Persistent: warp w normalises the contiguous rows [w*R, (w+1)*R), loading row i+1 before it
-// reduces row i so that two rows of loads are in flight per warp.  amax (optional): per-item
-// absmax of the bf16 outputs, item = row / rows_per_item, one atomic per warp and item.
+// reduces row i so that two rows of loads are in flight per warp.
 template <int NV, int VEC, bool RES, bool RMS>
 __global__ void __launch_bounds__(LN_WARPS * 32)
     layernorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
                      const float* __restrict__ g, const float* __restrict__ bta, int rows, float eps,
-                     __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ total, float* __restrict__ amax,
-                     int rows_per_item) {
+                     __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ total) {
   constexpr int D = NV * VEC * 32;
   using V = typename VecIO<VEC>::T;
   const int lane = threadIdx.x & 31;
@@ -205,8 +203,6 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   const long long r1 = r0 + per < rows ? r0 + per : rows;
   V u[NV], ur[NV], nu[NV], nur[NV];
   if (r0 < r1) ln_load<NV, VEC, RES>(x, res, r0, lane, u, ur);
-  float run_max = 0.0f;
-  int run_item = r0 < r1 ? static_cast<int>(r0 / rows_per_item) : 0;
   for (long long row = r0; row < r1; ++row) {
     if (row + 1 < r1) ln_load<NV, VEC, RES>(x, res, row + 1, lane, nu, nur);
     float v[NV * VEC];
@@ -246,7 +242,6 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
     const float rstd = rsqrtf(q * (1.0f / D) + eps);
-    float mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int off = (i * 32 + lane) * VEC;
@@ -266,34 +261,14 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
         const float y0 = fmaf((v[i * VEC + 2 * j] - mean) * rstd, gg[2 * j], bb[2 * j]);
         const float y1 = fmaf((v[i * VEC + 2 * j + 1] - mean) * rstd, gg[2 * j + 1], bb[2 * j + 1]);
         o32[j] = pack_bf16(y0, y1);
-        if (amax) {
-          const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&o32[j]);
-          mx = fmaxf(mx, fmaxf(fabsf(__bfloat162float(hv.x)), fabsf(__bfloat162float(hv.y))));
-        }
       }
       *reinterpret_cast<V*>(y + row * D + off) = o;
-    }
-    if (amax) {
-      const int item = static_cast<int>(row / rows_per_item);
-      if (item != run_item) {     // rows are contiguous per warp: items change rarely
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) run_max = fmaxf(run_max, __shfl_xor_sync(0xffffffffu, run_max, o));
-        if (lane == 0 && run_max > 0.0f) atomic_max_nonneg(amax + run_item, run_max);
-        run_max = 0.0f;
-        run_item = item;
-      }
-      run_max = fmaxf(run_max, mx);
     }
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       u[i] = nu[i];
       if (RES) ur[i] = nur[i];
     }
-  }
-  if (amax && r0 < r1) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) run_max = fmaxf(run_max, __shfl_xor_sync(0xffffffffu, run_max, o));
-    if (lane == 0 && run_max > 0.0f) atomic_max_nonneg(amax + run_item, run_max);
   }
 }
 
@@ -775,28 +750,26 @@ cudaError_t launch_pack_conv(const float* w, int c_out, int c_in, __nv_bfloat16*
 
 template <int NV, int VEC, bool RMS>
 static cudaError_t ln_launch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
-                             int rows, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             int rows_per_item, cudaStream_t s) {
+                             int rows, float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s) {
   // persistent grid: 2 blocks of 8 warps per SM, each warp walking a contiguous range of rows
   long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
   const long long cap = 2LL * sm_count();
   if (blocks > cap) blocks = cap;
   if (res)
     layernorm_kernel<NV, VEC, true, RMS><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
-        x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
+        x, res, g, b, rows, eps, y, total);
   else
     layernorm_kernel<NV, VEC, false, RMS><<<static_cast<int>(blocks), LN_WARPS * 32, 0, s>>>(
-        x, res, g, b, rows, eps, y, total, amax, rows_per_item > 0 ? rows_per_item : rows);
+        x, res, g, b, rows, eps, y, total);
   return cudaGetLastError();
 }
 
 template <bool RMS>
 static cudaError_t norm_dispatch(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
-                                 int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                                 int rows_per_item, cudaStream_t s) {
+                                 int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s) {
 #define WB_LN_CASE(NV, VEC) \
   case NV * VEC * 32:       \
-    return ln_launch<NV, VEC, RMS>(x, res, g, b, rows, eps, y, total, amax, rows_per_item, s);
+    return ln_launch<NV, VEC, RMS>(x, res, g, b, rows, eps, y, total, s);
   switch (d) {
     WB_LN_CASE(1, 4)
     WB_LN_CASE(1, 8)
@@ -861,14 +834,13 @@ cudaError_t launch_layernorm_e4m3(const __nv_bfloat16* x, const float* g, const 
 }
 
 cudaError_t launch_layernorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, const float* b,
-                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, float* amax,
-                             int rows_per_item, cudaStream_t s) {
-  return norm_dispatch<false>(x, res, g, b, rows, d, eps, y, total, amax, rows_per_item, s);
+                             int rows, int d, float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s) {
+  return norm_dispatch<false>(x, res, g, b, rows, d, eps, y, total, s);
 }
 
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, const float* g, int rows, int d,
                            float eps, __nv_bfloat16* y, __nv_bfloat16* total, cudaStream_t s) {
-  return norm_dispatch<true>(x, res, g, nullptr, rows, d, eps, y, total, nullptr, 0, s);
+  return norm_dispatch<true>(x, res, g, nullptr, rows, d, eps, y, total, s);
 }
 
 template <int NK>
