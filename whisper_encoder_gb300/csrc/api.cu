@@ -275,7 +275,7 @@ MelLayout mel_layout(int n_chunks) {
 }
 
 struct StemLayout {
-  size_t yTp, y1p, total;
+  size_t yTp, y1p, pos, total;
 };
 
 StemLayout stem_layout(const wb_dims* d, int batch) {
@@ -283,6 +283,7 @@ StemLayout stem_layout(const wb_dims* d, int batch) {
   StemLayout L;
   L.yTp = c.take(static_cast<size_t>(batch) * (N_FRAMES + 2) * d->n_mels * 2);
   L.y1p = c.take(static_cast<size_t>(batch) * (N_FRAMES + 1) * d->d_model * 2);
+  L.pos = c.take(static_cast<size_t>(T_TOK) * d->d_model * sizeof(float));   // position table
   L.total = c.off;
   return L;
 }
@@ -481,11 +482,13 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto* yTp = reinterpret_cast<__nv_bfloat16*>(ws + L.yTp);
   auto* y1p = reinterpret_cast<__nv_bfloat16*>(ws + L.y1p);
+  auto* pos = reinterpret_cast<float*>(ws + L.pos);
   const int C = dims->n_mels, D = dims->d_model;
 
   {
-    Prof pr(PC_STEM_PREP, s, 4);
+    Prof pr(PC_STEM_PREP, s, 5);
     WB_CUDA(launch_stem_transpose(logmel, batch, C, yTp, s));
+    WB_CUDA(launch_pos_table(pos, T_TOK, D, s));
     WB_CUDA(launch_zero_rows(y1p, D, static_cast<long long>(N_FRAMES + 1) * D, batch, 0, s));
   }
   {  // conv1: three taps = three passes over row-shifted views of yTp
@@ -538,6 +541,7 @@ wb_status wb_conv_stem(const float* logmel, int batch, const wb_dims* dims, cons
     p.n_pass = 3;
     if (!o_map(&g.omap, x0, D, T_TOK, batch, D, static_cast<uint64_t>(T_TOK) * D)) return WB_ECUDA;
     p.bias = w->conv2_b;
+    p.pos = pos;
     g.p = p;
     Prof pr(PC_STEM_CONV2, s);
     WB_CUDA(launch_gemm(g, s));

@@ -41,14 +41,6 @@ struct GemmSmem {
   static constexpr int TOTAL = 1024 + OFF_BAR + BAR_BYTES;
 };
 
-__device__ __forceinline__ float sinusoid(int t, int n, int d) {
-  const int half = d >> 1;
-  const int i = n < half ? n : n - half;
-  const float inc = 9.210340371976184f / static_cast<float>(half - 1);  // ln(10000) / (d/2 - 1)
-  const float ang = static_cast<float>(t) * expf(-inc * static_cast<float>(i));
-  return n < half ? sinf(ang) : cosf(ang);
-}
-
 // Byte offset of 16-byte chunk j (columns 8j..8j+7) of row r in a 32 x 64-byte box stored with
 // the 64-byte swizzle (chunk index XOR address bits 7-8), as TMA reads and writes it.
 __device__ __forceinline__ uint32_t box_off(int r, int j) {
@@ -292,9 +284,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   gelu_fast_x2(x0, x1);
                 }
               }
-              if (EPI == EPI_CONV2) {
-                x0 += sinusoid(m, n0 + 4 * i4 + kk, p.N);
-                x1 += sinusoid(m, n0 + 4 * i4 + kk + 1, p.N);
+              if (EPI == EPI_CONV2) {   // positional embedding from the table (row m, this column pair)
+                const int mr = row_ok ? m : p.M - 1;      // rows past M are not stored; stay inside the table
+                const float2 pe = __ldg(reinterpret_cast<const float2*>(p.pos + static_cast<long long>(mr) * p.N + n0 +
+                                                                        4 * i4 + kk));
+                x0 += pe.x;
+                x1 += pe.y;
               }
               v[4 * i4 + kk] = x0;
               v[4 * i4 + kk + 1] = x1;

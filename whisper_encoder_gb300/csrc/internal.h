@@ -58,6 +58,7 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, 
                                cudaStream_t s);
 cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long batch_stride_elems,
                              int batch, int row, cudaStream_t s);
+cudaError_t launch_pos_table(float* pos, int T, int d, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint32_t site, cudaStream_t s);
 
 // Launch with programmatic stream serialization: the kernel may begin (its prologue, up to its

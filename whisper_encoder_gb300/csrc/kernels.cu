@@ -938,6 +938,19 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, 
   return cudaGetLastError();
 }
 
+// pos[t][n] = sinusoid(t, n, d): the conv stem's position table, [T][d] float32.
+__global__ void pos_table_kernel(float* __restrict__ pos, int T, int d) {
+  const long long n_el = static_cast<long long>(T) * d;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_el; i += step)
+    pos[i] = sinusoid(static_cast<int>(i / d), static_cast<int>(i % d), d);
+}
+
+cudaError_t launch_pos_table(float* pos, int T, int d, cudaStream_t s) {
+  pos_table_kernel<<<grid_for(static_cast<long long>(T) * d, EW_THREADS), EW_THREADS, 0, s>>>(pos, T, d);
+  return cudaGetLastError();
+}
+
 // Diagnostic of the bounded-wait path: one thread waits on an mbarrier that
 // nothing ever arrives on.  mbar_wait gives up after its time limit, records
 // ERR_TIMEOUT with the site in the device error word and the kernel returns

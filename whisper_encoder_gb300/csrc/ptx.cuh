@@ -365,6 +365,16 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 
+// Whisper's sinusoidal position embedding, element (position t, channel n) of a d-wide table:
+// sin(t / 10000^(i / (d/2 - 1))) for n = i < d/2, the cosine for n = d/2 + i.
+__device__ __forceinline__ float sinusoid(int t, int n, int d) {
+  const int half = d >> 1;
+  const int i = n < half ? n : n - half;
+  const float inc = 9.210340371976184f / static_cast<float>(half - 1);  // ln(10000) / (d/2 - 1)
+  const float ang = static_cast<float>(t) * expf(-inc * static_cast<float>(i));
+  return n < half ? sinf(ang) : cosf(ang);
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

@@ -21,7 +21,7 @@ enum EpiKind : int {
   EPI_BIAS = 0,        // y = alpha*acc + bias                     (QKV with the V^T side output, plain linear)
   EPI_BIAS_GELU = 1,   // y = GELU(alpha*acc + bias)               (FC1, conv1)
   EPI_BIAS_RESID = 2,  // y = [GELU](alpha*acc + bias) + resid     (out-proj, FC2)
-  EPI_CONV2 = 3,       // y = GELU(acc + bias) + sinusoid(row, col) (conv2)
+  EPI_CONV2 = 3,       // y = GELU(acc + bias) + pos[row][col] (conv2, sinusoidal position table)
   EPI_POWER = 4,       // DFT: |X|^2 split into bf16 hi/lo parts
   EPI_MEL = 5          // mel: log10(max(acc, 1e-10)) written transposed, per-item max
 };
@@ -56,6 +56,7 @@ struct GemmParams {
   const float2* ln_stats;
   const float* ln_c;
   float* amax;               // if set: per-item atomic max of |y| (feeds the next E4M3 operand's scale)
+  const float* pos;          // EPI_CONV2: position table [M][N] (float32), added after the GELU
   // QKV: columns >= vt_col0 are written transposed, as f16, to vt[(b*H + h)*64 + e][t]
   __half* vt;
   int vt_col0, vt_T, vt_ld;  // tokens per batch item, elements between vt rows
