@@ -14,9 +14,8 @@
 // accumulates tile i+1.  Epilogue warp w owns TMEM lane quarter w%4 (32 rows)
 // and one quarter of the tile's columns; it stages its 32x32 output boxes in
 // shared memory and writes them with TMA bulk stores.  The residual of the
-// residual epilogue is read with plain 16-byte global loads, one 32-column
-// chunk ahead of its use (the first before the accumulator is ready).  All
-// waits are bounded.
+// residual epilogue is read with plain 16-byte global loads, all of a thread's
+// columns issued before the accumulator is ready.  All waits are bounded.
 //
 // K schedule: a list of passes; pass p reads A through tensor map amap[p]
 // (4-D: k, row, part, batch) at row offset a_row_off and part a_part, and B
@@ -201,19 +200,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int m = m0 + lane;
       const bool row_ok = m < p.M;
       const int ncol0 = nt * BN + cg * COLS;
-      // residual of this thread's row, 32 columns (64 bytes) per chunk, loaded one chunk ahead
-      uint4 rnext[4];
-      auto load_resid = [&](int n0) {
+      // residual of this thread's row: all CHUNKS x 32 columns (64 bytes each) loaded before the
+      // accumulator is ready, so their latency hides behind the main loop
+      uint4 rres[EPI == EPI_BIAS_RESID ? CHUNKS * 4 : 1];
+      if constexpr (EPI == EPI_BIAS_RESID) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) rnext[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (row_ok && n0 < p.N) {
-          const uint4* rp = reinterpret_cast<const uint4*>(
-              p.resid + b * p.resid_item + static_cast<long long>(p.out_row_off + m) * p.resid_ld + n0);
+        for (int c = 0; c < CHUNKS; ++c) {
+          const int n0 = ncol0 + c * 32;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) rnext[j] = rp[j];
+          for (int j = 0; j < 4; ++j) rres[4 * c + j] = make_uint4(0u, 0u, 0u, 0u);
+          if (row_ok && n0 < p.N) {
+            const uint4* rp = reinterpret_cast<const uint4*>(
+                p.resid + b * p.resid_item + static_cast<long long>(p.out_row_off + m) * p.resid_ld + n0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rres[4 * c + j] = rp[j];
+          }
         }
-      };
-      if (EPI == EPI_BIAS_RESID) load_resid(ncol0);
+      }
       // folded LayerNorm: this row's (mean, rstd), fetched while the accumulator is still being computed
       const bool lnf = (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) && !FP8 && p.ln_stats != nullptr;
       float2 ln_mr = make_float2(0.0f, 1.0f);
@@ -244,12 +247,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is free for tile i+2
           }
           if (n0 >= p.N) continue;
-          uint4 rcur[4];
-          if (EPI == EPI_BIAS_RESID) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) rcur[j] = rnext[j];
-            if (c + 1 < CHUNKS) load_resid(n0 + 32);
-          }
+
           // bias (+ E4M3 scale) and activation
           const float4* bp = reinterpret_cast<const float4*>(p.bias + n0);
           const float4* cp = reinterpret_cast<const float4*>(p.ln_c + n0);
@@ -309,10 +307,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             continue;
           }
-          if (EPI == EPI_BIAS_RESID) {
+          if constexpr (EPI == EPI_BIAS_RESID) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&rcur[j]);
+              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&rres[4 * c + j]);
 #pragma unroll
               for (int i = 0; i < 8; ++i) v[8 * j + i] += __bfloat162float(hv[i]);
             }
