@@ -8,7 +8,7 @@ second (RTFx).  Under torchrun every rank runs an independent replica on its
 own 32 chunks (no data-path collective; weak scaling); the host-side barrier
 and a MAX all-reduce of the elapsed time are the only cross-rank traffic.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--precision bf16|mixed_fp8]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--precision bf16|mixed_fp8|aggressive_fp8]
                     [--batch B] [--impl wb|reference]
 
 --impl reference times the float64 CPU oracle (the reference arm of this
@@ -72,6 +72,8 @@ def bytes_per_chunk(dims, precision: str = "bf16") -> dict:
         out["enc.layernorm"] = 2 * L * (row + row / 2) + 2 * row
         # E4M3 copy of the FC2 input ([1500, F]): read bf16, write u8
         out["enc.quantize"] = L * (T * F * 2.0 + T * F)
+        if precision == "aggressive_fp8":   # and of the out-projection input (read bf16, write u8)
+            out["enc.quantize"] += L * (row + row / 2)
     return out
 
 
@@ -336,7 +338,7 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--batch", type=int, default=32)
-    ap.add_argument("--precision", choices=("bf16", "mixed_fp8"), default="bf16")
+    ap.add_argument("--precision", choices=("bf16", "mixed_fp8", "aggressive_fp8"), default="bf16")
     ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph of the three calls")
@@ -373,7 +375,8 @@ def main() -> None:
 
     dims = synthetic.LARGE_V3
     B = args.batch
-    precision = wb.PRESET_BF16 if args.precision == "bf16" else wb.PRESET_MIXED_FP8
+    precision = {"bf16": wb.PRESET_BF16, "mixed_fp8": wb.PRESET_MIXED_FP8,
+                 "aggressive_fp8": wb.PRESET_AGGRESSIVE_FP8}[args.precision]
     seed = synthetic.SEED_LARGE_B32
     host_w = synthetic.encoder_weights(dims, seed, "bf16")
     stem, enc = wb.upload_weights(host_w)
@@ -469,7 +472,8 @@ def main() -> None:
                          "share": round(ms / max(total_ms, 1e-9), 4)}
         if name in fl:
             kernels[name]["tflops"] = round(fl[name] * B / (per_step_ms / 1000.0) / 1e12, 1)
-    fp8_classes = {"enc.qkv", "enc.fc1", "enc.fc2"} if args.precision == "mixed_fp8" else set()
+    fp8_classes = {"mixed_fp8": {"enc.qkv", "enc.fc1", "enc.fc2"},
+                   "aggressive_fp8": {"enc.qkv", "enc.out_proj", "enc.fc1", "enc.fc2"}}.get(args.precision, set())
     tensor_classes = [c for c in prof if c in fl]
     roofline = None
     if tensor_classes:

@@ -290,7 +290,7 @@ StemLayout stem_layout(const wb_dims* d, int batch) {
 
 // Attention over q/k row views (row stride ld_qk elements) and V^T.
 wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long long ld_qk, const __half* vt,
-                        int batch, int T, int H, __nv_bfloat16* out, cudaStream_t s) {
+                        int batch, int T, int H, __nv_bfloat16* out, cudaStream_t s, float* amax = nullptr) {
   const uint64_t d = static_cast<uint64_t>(H) * 64;
   CUtensorMap qm, km, vm;
   const uint64_t qdims[3] = {d, static_cast<uint64_t>(T), static_cast<uint64_t>(batch)};
@@ -309,6 +309,7 @@ wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long lon
   p.batch = batch;
   p.scale_log2 = 1.4426950408889634f / 8.0f;
   p.out = out;
+  p.amax = amax;
   p.err = err_ptr();
   Prof pr(PC_ENC_ATTN, s);
   WB_CUDA(launch_attention(qm, km, vm, p, s));
@@ -658,12 +659,12 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
       if (st != WB_OK) return st;
     }
     {
-      wb_status st = run_attention(qk, qk + D, 2 * D, vt, batch, T_TOK, H, o, s);
+      // an E4M3 out-projection operand takes its per-chunk absmax from the attention epilogue
+      wb_status st = run_attention(qk, qk + D, 2 * D, vt, batch, T_TOK, H, o, s, o8 ? am_out : nullptr);
       if (st != WB_OK) return st;
     }
     if (o8) {
-      Prof pr(PC_ENC_QUANT, s, 2);
-      WB_CUDA(launch_amax_items(o, static_cast<long long>(M) * D, D, T_TOK, am_out, s));
+      Prof pr(PC_ENC_QUANT, s);
       WB_CUDA(launch_quantize_rows(o, static_cast<long long>(M) * D, D, T_TOK, am_out, aq, s));
     }
     {  // out projection + bias + residual -> h

@@ -336,14 +336,25 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
       const int qa = q0 + ra, qb = qa + 8;
       __nv_bfloat16* oa = p.out + (static_cast<long long>(b) * p.T + qa) * p.d + h * ATT_HD + cq;
       __nv_bfloat16* ob = oa + 8LL * p.d;
+      uint32_t mx2 = 0u;                           // packed |bf16| maxima of the stored outputs
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        if (qa < p.T)
-          *reinterpret_cast<uint32_t*>(oa + 8 * kk) =
-              pack_bf16(__uint_as_float(v[4 * kk]) * ia, __uint_as_float(v[4 * kk + 1]) * ia);
-        if (qb < p.T)
-          *reinterpret_cast<uint32_t*>(ob + 8 * kk) =
-              pack_bf16(__uint_as_float(v[4 * kk + 2]) * ib, __uint_as_float(v[4 * kk + 3]) * ib);
+        const uint32_t wa = pack_bf16(__uint_as_float(v[4 * kk]) * ia, __uint_as_float(v[4 * kk + 1]) * ia);
+        const uint32_t wb = pack_bf16(__uint_as_float(v[4 * kk + 2]) * ib, __uint_as_float(v[4 * kk + 3]) * ib);
+        if (qa < p.T) {
+          *reinterpret_cast<uint32_t*>(oa + 8 * kk) = wa;
+          mx2 = bf16x2_max(mx2, wa & 0x7fff7fffu);
+        }
+        if (qb < p.T) {
+          *reinterpret_cast<uint32_t*>(ob + 8 * kk) = wb;
+          mx2 = bf16x2_max(mx2, wb & 0x7fff7fffu);
+        }
+      }
+      if (p.amax) {   // one atomic per warp: the per-chunk scale of an E4M3 out-projection operand
+        float mx = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xffff0000u));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0 && mx > 0.0f) atomic_max_nonneg(p.amax + b, mx);
       }
     }
   }

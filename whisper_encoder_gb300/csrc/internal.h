@@ -46,8 +46,6 @@ cudaError_t launch_dequantize_e5m2(const uint8_t* q, const float* scale, long lo
                                    cudaStream_t s);
 cudaError_t launch_quantize_rows(const __nv_bfloat16* x, long long n, int cols, int rows_per_item,
                                  const float* amax, uint8_t* q, cudaStream_t s);
-cudaError_t launch_amax_items(const __nv_bfloat16* x, long long n, int cols, int rows_per_item, float* amax,
-                              cudaStream_t s);
 cudaError_t launch_amax(const __nv_bfloat16* x, long long n, float* amax, cudaStream_t s);
 cudaError_t launch_quantize(const __nv_bfloat16* x, long long n, uint8_t* q, const float* amax,
                             float* scale_out, cudaStream_t s);

@@ -600,35 +600,6 @@ __global__ void quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, long l
   }
 }
 
-// Per-item absmax of a [rows, cols] bf16 tensor (item = row / rows_per_item), 8 elements per step.
-__global__ void amax_items_kernel(const __nv_bfloat16* __restrict__ x, long long n, int cols, int rows_per_item,
-                                  float* __restrict__ amax) {
-  const long long n8 = n / 8;
-  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long base = blockIdx.x * static_cast<long long>(blockDim.x); base < n8; base += step) {
-    const long long i = base + threadIdx.x;
-    float m = 0.0f;
-    int item = -1;
-    if (i < n8) {
-      item = static_cast<int>((i * 8) / cols / rows_per_item);
-      uint4 u = reinterpret_cast<const uint4*>(x)[i];
-      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(__bfloat162float(h[j])));
-    }
-    const int item0 = __shfl_sync(0xffffffffu, item, 0);
-    if (__all_sync(0xffffffffu, item == item0)) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if ((threadIdx.x & 31) == 0 && item0 >= 0 && m > 0.0f) atomic_max_nonneg(amax + item0, m);
-    } else if (item >= 0 && m > 0.0f) {
-      atomic_max_nonneg(amax + item, m);
-    }
-  }
-  (void)tid;
-}
-
 // E5M2 per-tensor cast: code = E5M2_rn_satfinite(x * 57344 / amax) (1 if amax == 0).
 __global__ void quantize_e5m2_kernel(const __nv_bfloat16* __restrict__ x, long long n, uint8_t* __restrict__ q,
                                      const float* __restrict__ amax) {
@@ -896,12 +867,6 @@ cudaError_t launch_quantize_rows(const __nv_bfloat16* x, long long n, int cols, 
                                  const float* amax, uint8_t* q, cudaStream_t s) {
   quantize_rows_kernel<<<grid_for(n / 16 + 1, EW_THREADS, 152 * 16), EW_THREADS, 0, s>>>(x, n, cols, rows_per_item,
                                                                                         amax, q);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_amax_items(const __nv_bfloat16* x, long long n, int cols, int rows_per_item, float* amax,
-                              cudaStream_t s) {
-  amax_items_kernel<<<grid_for(n / 8 + 1, EW_THREADS, 152 * 8), EW_THREADS, 0, s>>>(x, n, cols, rows_per_item, amax);
   return cudaGetLastError();
 }
 

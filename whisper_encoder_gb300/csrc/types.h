@@ -102,6 +102,7 @@ struct AttnParams {
   int batch;
   float scale_log2; // log2(e) / sqrt(64)
   __nv_bfloat16* out;  // [batch * T, d]
+  float* amax;         // if set: amax[b] = max |bf16 output| over batch item b (atomic; for an E4M3 scale)
   uint32_t* err;
 };
 
