@@ -817,7 +817,7 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, con
 template <int NK>
 static cudaError_t ln_stats_launch(const __nv_bfloat16* x, int rows, float eps, float2* out, cudaStream_t s) {
   long long blocks = (rows + LN_WARPS - 1) / LN_WARPS;
-  const long long cap = 2LL * sm_count();
+  const long long cap = 3LL * sm_count();   // 80 registers: three blocks of eight warps fit an SM
   if (blocks > cap) blocks = cap;
   return launch_pdl(ln_stats_amax_kernel<NK, false>, dim3(static_cast<unsigned>(blocks)), dim3(LN_WARPS * 32), 0, s, x,
                     static_cast<const float*>(nullptr), static_cast<const float*>(nullptr), rows, eps, out,
