@@ -79,15 +79,26 @@ def dequantize(codes, scale) -> np.ndarray:
 
 
 def round_bf16(x) -> np.ndarray:
-    """Round to bfloat16 (nearest, ties to even) and return the values as float64.
+    """Round each value once to bfloat16 and return the results as float64.
 
     An activation is stored as bf16 before it is quantised, so the quantisation
-    decision is taken on the bf16 value (the precision the GPU path stores).
+    decision is taken on the bf16 value.  bfloat16 (the format of the Google
+    Brain float and of the Arm / Intel ISA extensions that adopted it): sign, the
+    8 exponent bits of IEEE binary32, 7 stored significand bits, so 8
+    significant bits, subnormals spaced 2^-133 apart below 2^-126, largest
+    finite magnitude (2 - 2^-7) * 2^127.  Rounding is to nearest, ties to the
+    even significand, applied to the exact input value (no intermediate
+    float32 rounding); magnitudes that round past the largest finite value
+    become infinities; +-inf and NaN pass through.
     """
-    x32 = np.ascontiguousarray(x, dtype=np.float32)
-    u = x32.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        x = np.asarray(x, dtype=np.float64)
+        m, e = np.frexp(x)                                   # x = m * 2^e, 0.5 <= |m| < 1
+        normal = np.rint(m * 256.0) * np.exp2(e.astype(np.float64) - 8.0)   # 8 significant bits
+        sub = np.rint(x * 2.0 ** 133) * 2.0 ** -133                         # fixed spacing below 2^-126
+        r = np.where(np.abs(x) < 2.0 ** -126, sub, normal)
+        r = np.where(np.abs(r) >= 2.0 ** 128, np.copysign(np.inf, x), r)
+    return np.where(np.isfinite(x), r, x)
 
 
 def fake_quantize(x) -> np.ndarray:

@@ -89,3 +89,101 @@ def test_e5m2_encode_roundtrip_midpoints_and_saturation():
     x = np.random.default_rng(2).normal(0, 3000, 100000).astype(np.float32)
     x = x[np.abs(x) < 57000]
     np.testing.assert_array_equal(fp8.e5m2_encode(x), torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy())
+
+
+# --- bfloat16 storage rounding (the value an E4M3 site quantises) -----------------------------------
+
+def _bits_to_f32(bits):
+    return np.asarray(bits, dtype=np.uint32).view(np.float32)
+
+
+def test_round_bf16_matches_torch_over_all_exponents():
+    # float32 inputs are rounded once by both sides, so torch's cast is an independent reference
+    rng = np.random.default_rng(3)
+    mant = rng.integers(0, 1 << 23, size=400000, dtype=np.uint32)
+    expo = rng.integers(0, 255, size=400000, dtype=np.uint32)          # every biased exponent incl. 0
+    sign = rng.integers(0, 2, size=400000, dtype=np.uint32) << 31
+    x = _bits_to_f32(sign | (expo << 23) | mant)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(fp8.round_bf16(x), ref)
+
+
+def test_round_bf16_ties_go_to_the_even_significand():
+    # low 16 bits exactly 0x8000: halfway between two bf16 values
+    hi = np.arange(0x3F80, 0x3F90, dtype=np.uint32)                     # 1.0 .. 1.0 + 15 * 2^-7
+    ties = _bits_to_f32((hi << 16) | 0x8000)
+    expect = _bits_to_f32(((hi + (hi & 1)) << 16)).astype(np.float64)   # odd rounds up, even stays
+    np.testing.assert_array_equal(fp8.round_bf16(ties), expect)
+    np.testing.assert_array_equal(fp8.round_bf16(-ties), -expect)
+    ref = torch.from_numpy(ties).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(fp8.round_bf16(ties), ref)
+    # one unit past the tie rounds away from it whatever the parity
+    np.testing.assert_array_equal(fp8.round_bf16(_bits_to_f32((hi << 16) | 0x8001)),
+                                  _bits_to_f32((hi + 1) << 16).astype(np.float64))
+
+
+def test_round_bf16_rounds_the_exact_value_once():
+    # 1 + 2^-8 + 2^-40 lies just above the tie between 1 and 1 + 2^-7: nearest is 1 + 2^-7.
+    # Rounding it to float32 first would land exactly on the tie and then go to the even 1.0.
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert fp8.round_bf16(x) == 1.0 + 2.0 ** -7
+    assert fp8.round_bf16(1.0 + 2.0 ** -8) == 1.0
+    assert fp8.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6       # tie, odd -> up to even
+
+
+def test_round_bf16_subnormals_overflow_and_specials():
+    tiny = 2.0 ** -133                                                    # smallest bf16 subnormal
+    assert fp8.round_bf16(tiny) == tiny and fp8.round_bf16(0.5 * tiny) == 0.0    # tie -> even (0)
+    assert fp8.round_bf16(0.75 * tiny) == tiny and fp8.round_bf16(1.5 * tiny) == 2 * tiny
+    assert fp8.round_bf16(2.0 ** -126 - tiny) == 2.0 ** -126 - tiny       # largest subnormal is exact
+    big = (2.0 - 2.0 ** -7) * 2.0 ** 127                                  # largest finite bf16
+    assert fp8.round_bf16(big) == big
+    assert fp8.round_bf16(big + 2.0 ** 119) == np.inf                     # halfway to 2^128: tie -> even -> inf
+    assert fp8.round_bf16(big + 2.0 ** 118) == big
+    assert fp8.round_bf16(-np.inf) == -np.inf and np.isnan(fp8.round_bf16(np.nan))
+    assert np.signbit(fp8.round_bf16(-0.0)) and fp8.round_bf16(-0.0) == 0.0
+    assert np.isnan(fp8.round_bf16(_bits_to_f32(0x7F800001)))            # a NaN payload stays NaN
+
+
+def test_activation_site_matches_torch_dtypes():
+    # bf16 storage then per-tensor E4M3 (scale amax / 448), rebuilt from torch's bfloat16 and
+    # float8_e4m3fn casts; float32-valued input so that both sides round it once
+    rng = np.random.default_rng(4)
+    a = (rng.normal(size=(64, 96)) * 3.0).astype(np.float32)
+    got = fp8.fake_quantize(fp8.round_bf16(a))
+    t = torch.from_numpy(a).to(torch.bfloat16).to(torch.float32)
+    amax = t.abs().max()
+    inv = torch.tensor(448.0, dtype=torch.float32) / amax
+    codes = (t * inv).to(torch.float8_e4m3fn)
+    ref = codes.to(torch.float64) * (amax / torch.tensor(448.0, dtype=torch.float32)).to(torch.float64)
+    np.testing.assert_array_equal(got, ref.numpy())
+
+
+# --- E5M2 per-tensor scale recipe ----------------------------------------------------------------
+
+def test_quantize_e5m2_scale_recipe():
+    rng = np.random.default_rng(5)
+    x = (rng.normal(size=(200, 64)) * 40.0).astype(np.float32)
+    x[3, 9] = -1234.5                                                     # the absmax element
+    q, s = fp8.quantize_e5m2(x)
+    assert s == np.float32(1234.5) / np.float32(57344.0)                 # dequantisation scale
+    assert q[3, 9] == 0xFB                                                # -57344, the largest finite code
+    qn, sn = fp8.quantize_e5m2(-x)
+    assert sn == s and np.array_equal(qn, q ^ 0x80)                       # sign symmetry
+    deq = fp8.e5m2_decode(q) * np.float64(s)
+    big = np.abs(x) > 1e-3 * 1234.5                                       # away from the subnormal codes
+    rel = np.abs(deq - x)[big] / np.abs(x)[big]
+    assert rel.max() <= 2.0 ** -3 * (1 + 1e-6)                            # 2 significand bits: half-ulp <= 1/8
+    q0, s0 = fp8.quantize_e5m2(np.zeros((4, 4), np.float32))
+    assert s0 == 1.0 and (q0 == 0).all()
+
+
+def test_quantize_e5m2_matches_torch_dtype():
+    # the same recipe rebuilt from torch's float8_e5m2 cast
+    x = (np.random.default_rng(6).normal(size=(128, 80)) * 0.3).astype(np.float32)
+    q, s = fp8.quantize_e5m2(x)
+    t = torch.from_numpy(x)
+    amax = t.abs().max()
+    ref = (t * (torch.tensor(57344.0) / amax)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(q, ref)
+    assert s == (amax / torch.tensor(57344.0)).item()
