@@ -341,6 +341,8 @@ def main() -> None:
     ap.add_argument("--precision", choices=("bf16", "mixed_fp8", "aggressive_fp8"), default="bf16")
     ap.add_argument("--impl", choices=("wb", "reference"), default="wb")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mixed-fp8", action="store_true",
+                    help="skip the mixed_fp8 step timed after the bf16 one (bf16 runs only)")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph of the three calls")
     ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "layernorm_e4m3", "logmel",
                                        "longform"),
@@ -385,65 +387,108 @@ def main() -> None:
     audio = torch.from_numpy(audio_np).cuda()
     pipe = wb.Pipeline(dims, stem, enc, B, precision)
     stream = torch.cuda.current_stream()
-
-    step = (lambda: pipe(audio))  # noqa: E731
-    graph_launches = None
-    if args.graph:
-        wb.profile_begin()                       # count the library's launches in one eager step
-        pipe(audio)
-        torch.cuda.synchronize()
-        graph_launches = sum(n for _, n in wb.profile_end().values())
-        graph = pipe.capture(audio)
-        step = graph.replay
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if wb.check_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")   # > 129 MB L2
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(gpu_uuid(torch, local))
-    time.sleep(0.3)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    if not args.graph:
-        wb.profile_begin()
-    for k in range(args.steps):
-        flush.zero_()
-        starts[k].record(stream)
-        step()
-        stops[k].record(stream)
-    torch.cuda.synchronize()
-    prof = wb.profile_end() if not args.graph else {}
-    if dist is not None:
-        dist.barrier()
-    clocks = sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, stops)]
-    total_ms = sum(step_ms)
-    if wb.check_device_error() != 0:
-        raise RuntimeError("device error in the timed region")
+    peaks = load_peaks()
+    fl = flops_per_chunk(dims)
+
     def reduce_max(v: float) -> float:
         t = torch.tensor([v], dtype=torch.float64, device="cuda")
         if dist is not None:
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return t.item()
 
-    value, ms_step = job_throughput(total_ms, args.steps, B, world, reduce_max)
+    def timed(pipe_, graph_mode: bool) -> dict:
+        """Warm up, then time K steps (L2 flushed before each) with CUDA events on the launching
+        stream, the library's per-launch events and the clock sampler running."""
+        step = (lambda: pipe_(audio))  # noqa: E731
+        graph_launches = None
+        if graph_mode:
+            wb.profile_begin()                       # count the library's launches in one eager step
+            pipe_(audio)
+            torch.cuda.synchronize()
+            graph_launches = sum(n for _, n in wb.profile_end().values())
+            graph = pipe_.capture(audio)
+            step = graph.replay
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if wb.check_device_error() != 0:
+            raise RuntimeError("device error during warm-up")
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        sampler = ClockSampler(gpu_uuid(torch, local))
+        time.sleep(0.3)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        if not graph_mode:
+            wb.profile_begin()
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            stops[k].record(stream)
+        torch.cuda.synchronize()
+        prof = wb.profile_end() if not graph_mode else {}
+        if dist is not None:
+            dist.barrier()
+        clocks = sampler.stop()
+        total_ms = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, stops))
+        if wb.check_device_error() != 0:
+            raise RuntimeError("device error in the timed region")
+        value, ms_step = job_throughput(total_ms, args.steps, B, world, reduce_max)
+        launches = sum(n for _, n in prof.values()) if prof else graph_launches * args.steps
+        return {"value": value, "ms_step": ms_step, "total_ms": total_ms, "prof": prof, "clocks": clocks,
+                "gpu_launches": launches}
+
+    def analyse(res: dict, prec: str) -> dict:
+        """Per-class rates, the dominant tensor-core class against its peak, and the step roofline."""
+        prof, total_ms = res["prof"], res["total_ms"]
+        fp8_classes = {"mixed_fp8": {"enc.qkv", "enc.fc1", "enc.fc2"},
+                       "aggressive_fp8": {"enc.qkv", "enc.out_proj", "enc.fc1", "enc.fc2"}}.get(prec, set())
+        kernels = {}
+        for name, (ms, n) in prof.items():
+            per_step_ms = ms / args.steps
+            kernels[name] = {"ms_per_step": round(per_step_ms, 4), "launches_per_step": n // args.steps,
+                             "share": round(ms / max(total_ms, 1e-9), 4)}
+            if name in fl:
+                tf = fl[name] * B / (per_step_ms / 1000.0) / 1e12
+                pk = peaks["bf16_sustained"] * (2.0 if name in fp8_classes else 1.0)
+                kernels[name]["tflops"] = round(tf, 1)
+                kernels[name]["frac"] = round(tf / pk, 4)
+                kernels[name]["operands"] = "e4m3" if name in fp8_classes else "bf16"
+        roofline = None
+        tensor_classes = [c for c in prof if c in fl]
+        if tensor_classes:
+            dom = max(tensor_classes, key=lambda c: prof[c][0])
+            dom_ms, dom_n = prof[dom]
+            per_launch_ms = dom_ms / dom_n
+            flops_launch = fl[dom] * B / (dom_n / args.steps)
+            achieved = flops_launch / (per_launch_ms / 1000.0) / 1e12
+            peak = peaks["bf16_sustained"] * (2.0 if dom in fp8_classes else 1.0)
+            roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(dom),
+                        "flops_per_launch": flops_launch, "ms_per_launch": round(per_launch_ms, 4),
+                        "peak_source": f"{peaks['source']} bf16 sustained"
+                                       + (" x2 (E4M3 nominal ratio)" if dom in fp8_classes else "")}
+        step_roof = step_roofline(fl, bytes_per_chunk(dims, prec), B, peaks, fp8_classes, res["ms_step"])
+        return {"kernels": kernels, "roofline": roofline, "step_roofline": step_roof}
+
+    res = timed(pipe, args.graph)
+    value, ms_step = res["value"], res["ms_step"]
 
     # ---- end to end: pinned host audio in, encoder output back to pinned host memory, every step.
     # Eager: Pipeline.run_host overlaps each step's upload and download with its neighbours' compute
     # (two device buffers each, copy streams).  Graph: the captured buffers, copies in line.
     audio_host = torch.from_numpy(audio_np).pin_memory()
     out_host = torch.empty(pipe.out.shape, dtype=pipe.out.dtype).pin_memory()
+    graph_e2e = pipe.capture(audio) if args.graph else None
 
     def e2e_steps(k):
         if args.graph:
             for _ in range(k):
                 audio.copy_(audio_host, non_blocking=True)
-                step()
+                graph_e2e.replay()
                 out_host.copy_(pipe.out, non_blocking=True)
         else:
             pipe.run_host([audio_host] * k, [out_host] * k)
@@ -462,37 +507,8 @@ def main() -> None:
            "h2d_bytes_per_step": audio_host.numel() * audio_host.element_size(),
            "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
 
-    # ---- roofline of the dominant kernel class, from the events around each launch
-    peaks = load_peaks()
-    fl = flops_per_chunk(dims)
-    kernels = {}
-    for name, (ms, n) in prof.items():
-        per_step_ms = ms / args.steps
-        kernels[name] = {"ms_per_step": round(per_step_ms, 4), "launches_per_step": n // args.steps,
-                         "share": round(ms / max(total_ms, 1e-9), 4)}
-        if name in fl:
-            kernels[name]["tflops"] = round(fl[name] * B / (per_step_ms / 1000.0) / 1e12, 1)
-    fp8_classes = {"mixed_fp8": {"enc.qkv", "enc.fc1", "enc.fc2"},
-                   "aggressive_fp8": {"enc.qkv", "enc.out_proj", "enc.fc1", "enc.fc2"}}.get(args.precision, set())
-    tensor_classes = [c for c in prof if c in fl]
-    roofline = None
-    if tensor_classes:
-        dom = max(tensor_classes, key=lambda c: prof[c][0])
-        dom_ms, dom_n = prof[dom]
-        per_launch_ms = dom_ms / dom_n
-        flops_launch = fl[dom] * B / (dom_n / args.steps)
-        achieved = flops_launch / (per_launch_ms / 1000.0) / 1e12
-        peak = peaks["bf16_sustained"] * (2.0 if dom in fp8_classes else 1.0)
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(dom),
-                    "flops_per_launch": flops_launch, "ms_per_launch": round(per_launch_ms, 4),
-                    "peak_source": f"{peaks['source']} bf16 sustained"
-                                   + (" x2 (E4M3 nominal ratio)" if dom in fp8_classes else "")}
+    an = analyse(res, args.precision)
     step_flops = sum(fl.values()) * B
-    step_roof = step_roofline(fl, bytes_per_chunk(dims, args.precision), B, peaks, fp8_classes, ms_step)
-    # launches per step: counted by the library's own events (eager), or one graph launch
-    gpu_launches = sum(n for _, n in prof.values()) if prof else graph_launches * args.steps
-
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -500,9 +516,31 @@ def main() -> None:
         "impl": "wb",
         "config": arm_config(args, world),
         "tflops": round(step_flops / (ms_step / 1000.0) / 1e12, 1),
-        "roofline": roofline, "step_roofline": step_roof, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "graph": bool(args.graph),
-        "kernels": kernels,
+        "roofline": an["roofline"], "step_roofline": an["step_roofline"], "e2e": e2e,
+        "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "graph": bool(args.graph),
+        "kernels": an["kernels"],
     }
+
+    # ---- the same step with the mixed_fp8 preset (E4M3 operands at the qkv and ffn sites, one
+    # scale per chunk), same inputs, same number of steps, L2 flush and clock sampling
+    if args.precision == "bf16" and not args.graph and not args.no_mixed_fp8:
+        del pipe
+        torch.cuda.empty_cache()
+        pipe8 = wb.Pipeline(dims, stem, enc, B, wb.PRESET_MIXED_FP8)
+        res8 = timed(pipe8, False)
+        an8 = analyse(res8, "mixed_fp8")
+        gemm_fracs = {c: an8["kernels"][c]["frac"] for c in ("enc.qkv", "enc.out_proj", "enc.fc1", "enc.fc2")
+                      if c in an8["kernels"]}
+        line["mixed_fp8"] = {
+            "workload": workload_name(argparse.Namespace(batch=B, precision="mixed_fp8")),
+            "value": round(res8["value"], 2), "unit": UNIT, "ms_per_step": round(res8["ms_step"], 3),
+            "dtype": "bf16+e4m3", "tflops": round(step_flops / (res8["ms_step"] / 1000.0) / 1e12, 1),
+            "gemm_fracs": gemm_fracs,
+            "gemm_peaks": "E4M3 classes (qkv, fc1, fc2) against 2 x the measured sustained bf16 peak; "
+                          "out_proj (bf16 in mixed_fp8) against 1 x",
+            "roofline": an8["roofline"], "step_roofline": an8["step_roofline"],
+            "gpu_launches": res8["gpu_launches"], "clocks": res8["clocks"], "kernels": an8["kernels"]}
+        del pipe8
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, parts = oracle_chunk_seconds(dims, seed)
         line["cpu_baseline"] = {

@@ -17,6 +17,10 @@
  *  - Pointers must be 16-byte aligned.  bf16 tensors hold IEEE bfloat16 bit
  *    patterns; E4M3 tensors hold OCP FP8 E4M3 ("fn") codes.
  *  - Row-major layouts throughout; "[a, b]" means b is contiguous.
+ *  - libwb looks up a few device addresses of its own (the device error word,
+ *    the scratch array of wb_logmel_static) once per device and keeps them;
+ *    cudaDeviceReset() invalidates them, so a process must not call libwb on
+ *    a device after resetting it.
  *
  * Sources (the pages this library follows): the whisper-blaze PyPI page
  * ("Quick Start", "Batch Transcription", "Direct Kernel API") and the
@@ -159,6 +163,9 @@ wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride,
  *    anything is launched; other arguments as for wb_logmel.
  *  - The first call on a device, made with that device current, looks up the
  *    array's device address; make that first call before any stream capture.
+ *    The address is kept for the life of the process: after cudaDeviceReset()
+ *    of that device it is stale, so do not call this entry point on a device
+ *    that was reset in the same process.
  *  - All calls share the one array per device and it keeps the previous
  *    call's contents (the call clears what must start at zero itself).  Calls
  *    whose GPU work overlaps, e.g. on two streams without ordering, race on
@@ -198,6 +205,55 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
                              const wb_ln_weights* ln_post, const wb_precision* precision, int layer_begin,
                              int layer_end, int apply_final_ln, void* out, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/* --- end to end from host memory -------------------------------------------------
+ * The PyPI page, "Quick Start" and "Batch Transcription": the caller hands over float32
+ * 16 kHz audio held in HOST memory and receives the encoder's hidden states in HOST memory.
+ * wb_encode_host runs n_batches batches through wb_logmel, wb_conv_stem and
+ * wb_encoder_forward (layers 0 .. dims.n_layers - 1 and the final LayerNorm): for batch i,
+ * one cudaMemcpyAsync of host_audio[i] (samples_per_batch floats) into a device audio
+ * buffer, the three calls on `stream`, and one cudaMemcpyAsync of the bf16
+ * [batch, 1500, d] result into host_out[i].
+ *  - With upload_stream and download_stream set (both or neither), uploads and downloads
+ *    run on them, against two device audio and two device output buffers, so that the
+ *    copies of neighbouring batches overlap a batch's compute; CUDA events order each
+ *    buffer's reuse (the call creates and destroys 10 events; it allocates no memory).
+ *    With both NULL every copy runs in order on `stream` and only dev_audio[0] and
+ *    dev_out[0] are used.
+ *  - Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister): copies from
+ *    pageable memory are correct but do not overlap.
+ *  - Returns once everything is queued; all of it, the last download included, is ordered
+ *    before later work on `stream` (synchronize `stream` to wait for host_out).
+ *  - Every pointer in the struct is a DEVICE pointer owned by the caller, except the
+ *    weight structs (host structs holding device pointers) and the streams.  Workspaces as
+ *    the *_workspace_bytes() queries give for (dims, batch, precision).
+ *  - WB_EINVAL for a missing buffer or host pointer, n_batches < 0, or only one copy
+ *    stream; otherwise the status of the first call that fails (nothing after it is
+ *    queued; earlier batches may already be in flight). */
+typedef struct {
+  wb_dims dims;
+  int32_t batch;                  /* chunks per batch */
+  int64_t samples_per_batch;      /* floats per host_audio[i] (wb_logmel's n_samples) */
+  int64_t chunk_stride;           /* as for wb_logmel: 480000, or 400000 for 25 s strides */
+  const wb_stem_weights* stem;
+  const wb_layer_weights* layers; /* [dims.n_layers] */
+  const wb_ln_weights* ln_post;
+  wb_precision precision;
+  float* dev_audio[2];            /* f32 [samples_per_batch] each */
+  float* dev_mel;                 /* f32 [batch, n_mels, 3000] */
+  void* dev_x0;                   /* bf16 [batch, 1500, d] */
+  void* dev_out[2];               /* bf16 [batch, 1500, d] each */
+  void* ws_mel;                   /* wb_logmel_workspace_bytes(batch, n_mels) */
+  size_t ws_mel_bytes;
+  void* ws_stem;                  /* wb_conv_stem_workspace_bytes(&dims, batch) */
+  size_t ws_stem_bytes;
+  void* ws_enc;                   /* wb_encoder_workspace_bytes(&dims, batch, &precision) */
+  size_t ws_enc_bytes;
+  void* upload_stream;            /* cudaStream_t for host -> device copies, or NULL */
+  void* download_stream;          /* cudaStream_t for device -> host copies, or NULL */
+} wb_host_pipeline;
+wb_status wb_encode_host(const wb_host_pipeline* p, const float* const* host_audio, void* const* host_out,
+                         int n_batches, void* stream);
 
 /* --- FP8 E4M3 ------------------------------------------------------------------
  * PyPI page, "Direct Kernel API" (quantise_e4m3 / dequantise_e4m3) and the

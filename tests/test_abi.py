@@ -116,6 +116,37 @@ def test_argument_errors_return_before_any_launch(lib):
     assert lib.wb_layernorm_e4m3(None, None, None, 0, 256, 1e-5, 1, None, None, None, None) == _lib.WB_OK
 
 
+def test_encode_host_argument_errors(lib):
+    # host-side checks of wb_encode_host, all before any copy or launch is queued
+    from whisper_encoder_gb300 import _lib
+    import synthetic
+    d = synthetic.TINY
+    hp = _lib.wb_host_pipeline()
+    hp.dims = _lib.wb_dims(d.n_mels, d.d_model, d.n_heads, d.n_layers, d.d_ffn)
+    hp.batch, hp.samples_per_batch, hp.chunk_stride = 1, 480000, 480000
+    fake = 1 << 20
+    stem, ln = _lib.wb_stem_weights(fake, fake, fake, fake), _lib.wb_ln_weights(fake, fake)
+    layers = (_lib.wb_layer_weights * 1)()
+    hp.stem, hp.layers, hp.ln_post = ctypes.pointer(stem), layers, ctypes.pointer(ln)
+    hp.dev_audio[0] = hp.dev_audio[1] = hp.dev_out[0] = hp.dev_out[1] = fake
+    hp.dev_mel = hp.dev_x0 = fake
+    arr = (ctypes.c_void_p * 1)(fake)
+    enc = lib.wb_encode_host
+    assert enc(ctypes.byref(hp), arr, arr, 0, None) == _lib.WB_OK                 # nothing to do
+    assert enc(None, arr, arr, 1, None) == _lib.WB_EINVAL
+    assert enc(ctypes.byref(hp), arr, arr, -1, None) == _lib.WB_EINVAL
+    assert enc(ctypes.byref(hp), None, arr, 1, None) == _lib.WB_EINVAL            # no host audio
+    nulls = (ctypes.c_void_p * 1)(None)
+    assert enc(ctypes.byref(hp), arr, nulls, 1, None) == _lib.WB_EINVAL           # a missing host output
+    hp.upload_stream = fake                                                       # only one copy stream
+    assert enc(ctypes.byref(hp), arr, arr, 1, None) == _lib.WB_EINVAL
+    hp.download_stream = fake
+    hp.dev_out[1] = None                                                          # second buffer missing
+    assert enc(ctypes.byref(hp), arr, arr, 1, None) == _lib.WB_EINVAL
+    hp.batch = 0
+    assert enc(ctypes.byref(hp), arr, arr, 1, None) == _lib.WB_EINVAL
+
+
 def _imports(path):
     out = []
     for dirpath, _, files in os.walk(path):

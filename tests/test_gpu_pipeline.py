@@ -131,8 +131,10 @@ def test_tiny_mixed_fp8(wb):
     enc.quantize()
     out = to_np(wb.encoder_forward(x0d, dims, enc, precision=wb.PRESET_MIXED_FP8))[0]
     ref8 = oenc.encoder(to_np(x0d)[0], w, dims.n_heads, fp8_sites=oenc.MIXED_FP8)
-    assert rel_l2(out, ref8) < FP8_TOL
-    assert rel_l2(out, oenc.encoder(to_np(x0d)[0], w, dims.n_heads)) < 0.1
+    e8, e = rel_l2(out, ref8), rel_l2(out, oenc.encoder(to_np(x0d)[0], w, dims.n_heads))
+    print(f"tiny mixed_fp8: {e8:.3e} from the E4M3 oracle, {e:.3e} from the unquantised one")
+    assert e8 < FP8_TOL
+    assert e < 0.1
 
 
 def test_encoder_zero_layers_and_range(wb):

@@ -49,6 +49,15 @@ class wb_ln_weights(ctypes.Structure):
     _fields_ = [("g", c_void), ("b", c_void)]
 
 
+class wb_host_pipeline(ctypes.Structure):
+    _fields_ = [("dims", wb_dims), ("batch", ctypes.c_int32), ("samples_per_batch", ctypes.c_int64),
+                ("chunk_stride", ctypes.c_int64), ("stem", P(wb_stem_weights)), ("layers", P(wb_layer_weights)),
+                ("ln_post", P(wb_ln_weights)), ("precision", wb_precision), ("dev_audio", c_void * 2),
+                ("dev_mel", c_void), ("dev_x0", c_void), ("dev_out", c_void * 2), ("ws_mel", c_void),
+                ("ws_mel_bytes", c_size), ("ws_stem", c_void), ("ws_stem_bytes", c_size), ("ws_enc", c_void),
+                ("ws_enc_bytes", c_size), ("upload_stream", c_void), ("download_stream", c_void)]
+
+
 # name -> (restype, argtypes); must match include/wb.h
 SIGNATURES = {
     "wb_status_string": (ctypes.c_char_p, [c_int]),
@@ -64,6 +73,7 @@ SIGNATURES = {
     "wb_encoder_workspace_bytes": (c_size, [P(wb_dims), c_int, P(wb_precision)]),
     "wb_encoder_forward": (c_int, [c_void, c_int, P(wb_dims), P(wb_layer_weights), P(wb_ln_weights),
                                    P(wb_precision), c_int, c_int, c_int, c_void, c_void, c_size, c_void]),
+    "wb_encode_host": (c_int, [P(wb_host_pipeline), P(c_void), P(c_void), c_int, c_void]),
     "wb_quantize_fp8": (c_int, [c_void, c_i64, c_void, c_void, c_void]),
     "wb_fold_layernorm": (c_int, [c_void, c_void, c_void, c_void, c_int, c_int, c_void, c_void, c_void, c_void]),
     "wb_dequantize_fp8": (c_int, [c_void, c_void, c_i64, c_void, c_void]),

@@ -37,6 +37,14 @@ def _need(t, dtype, name):
         raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor")
 
 
+def _need_out(t, dtype, shape, device, name):
+    """A caller-supplied output must be exactly what the kernel writes: the kernels write every
+    element of the given shape and nothing is checked on the device."""
+    _need(t, dtype, name)
+    if tuple(t.shape) != tuple(shape) or t.device != device:
+        raise ValueError(f"{name}: expected shape {tuple(shape)} on {device}, got {tuple(t.shape)} on {t.device}")
+
+
 def _workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
@@ -60,6 +68,7 @@ def logmel(audio: torch.Tensor, n_chunks: int, n_mels: int, chunk_stride: int = 
     _need(audio, torch.float32, "audio")
     if out is None:
         out = torch.empty((n_chunks, n_mels, N_FRAMES), dtype=torch.float32, device=audio.device)
+    _need_out(out, torch.float32, (n_chunks, n_mels, N_FRAMES), audio.device, "out")
     if workspace is None:
         workspace = _workspace(logmel_workspace_bytes(n_chunks, n_mels), audio.device)
     call("wb_logmel", _p(audio), audio.numel(), chunk_stride, n_chunks, n_mels, _p(out), _p(workspace),
@@ -77,6 +86,7 @@ def logmel_static(audio: torch.Tensor, n_chunks: int, n_mels: int, chunk_stride:
     _need(audio, torch.float32, "audio")
     if out is None:
         out = torch.empty((n_chunks, n_mels, N_FRAMES), dtype=torch.float32, device=audio.device)
+    _need_out(out, torch.float32, (n_chunks, n_mels, N_FRAMES), audio.device, "out")
     call("wb_logmel_static", _p(audio), audio.numel(), chunk_stride, n_chunks, n_mels, _p(out), _stream(stream))
     return out
 
@@ -99,6 +109,7 @@ def conv_stem(mel: torch.Tensor, dims, stem: "StemWeights", out: torch.Tensor | 
     ds = dims_struct(dims)
     if out is None:
         out = torch.empty((batch, N_TOKENS, dims.d_model), dtype=torch.bfloat16, device=mel.device)
+    _need_out(out, torch.bfloat16, (batch, N_TOKENS, dims.d_model), mel.device, "out")
     if workspace is None:
         workspace = _workspace(load().wb_conv_stem_workspace_bytes(ctypes.byref(ds), batch), mel.device)
     call("wb_conv_stem", _p(mel), batch, ctypes.byref(ds), ctypes.byref(stem.struct()), _p(out), _p(workspace),
@@ -123,6 +134,7 @@ def encoder_forward(x0: torch.Tensor, dims, weights: "EncoderWeights", precision
     ds, pr = dims_struct(dims), precision_struct(precision)
     if out is None:
         out = torch.empty_like(x0)
+    _need_out(out, torch.bfloat16, tuple(x0.shape), x0.device, "out")
     if workspace is None:
         workspace = _workspace(encoder_workspace_bytes(dims, batch, precision), x0.device)
     layers = weights.layer_array(precision)
@@ -435,45 +447,47 @@ class Pipeline:
                         stream=stream)
         return dst[:n]
 
-    def run_host(self, host_in: list, host_out: list, chunk_stride: int = CHUNK_SAMPLES) -> None:
-        """Encode a sequence of full batches held in pinned host memory.
+    def run_host(self, host_in: list, host_out: list, chunk_stride: int = CHUNK_SAMPLES, overlap: bool = True) -> None:
+        """Encode a sequence of full batches held in pinned host memory through wb_encode_host.
 
         host_in[i]: pinned float32 audio of batch i (as for __call__); host_out[i]: pinned bf16
-        [batch, 1500, d] that receives batch i's encoder output.  Batch i's audio upload and result
-        download run on two copy streams, against two device input and two device output buffers,
-        so they overlap the compute of batches i-1 and i+1.  Returns with all work queued on the
-        current stream (synchronize it to wait for the last download)."""
-        comp = torch.cuda.current_stream()
+        [batch, 1500, d] that receives batch i's encoder output.  The library copies each batch up,
+        runs the three calls and copies the result back; with ``overlap`` the copies run on two
+        copy streams against two device input and two device output buffers, so they overlap
+        the compute of the neighbouring batches.  Returns with all work queued on the current
+        stream (synchronize it to wait for the last download)."""
+        n = len(host_in)
+        if len(host_out) != n:
+            raise ValueError("host_in and host_out differ in length")
+        if n == 0:
+            return
+        for t in host_in:
+            if t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous() or t.shape != host_in[0].shape:
+                raise ValueError("host_in: contiguous float32 host tensors of one shape expected")
+        for t in host_out:
+            if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(self.out.shape):
+                raise ValueError(f"host_out: contiguous bf16 host tensors of shape {tuple(self.out.shape)} expected")
         if not hasattr(self, "_copy"):
             self._copy = (torch.cuda.Stream(), torch.cuda.Stream())
             self._out2 = torch.empty_like(self.out)
             self._dev_in = None
-        up, down = self._copy
         if self._dev_in is None or self._dev_in[0].shape != host_in[0].shape:
             self._dev_in = [torch.empty(host_in[0].shape, dtype=torch.float32, device=self.out.device) for _ in range(2)]
-        outs = (self.out, self._out2)
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        in_free = [torch.cuda.Event() for _ in range(2)]
-        out_ready = [torch.cuda.Event() for _ in range(2)]
-        out_free = [torch.cuda.Event() for _ in range(2)]
-        up.wait_stream(comp)
-        down.wait_stream(comp)
-        for i, (hi, ho) in enumerate(zip(host_in, host_out)):
-            k = i % 2
-            if i >= 2:
-                up.wait_event(in_free[k])              # the compute that read this buffer is done
-            with torch.cuda.stream(up):
-                self._dev_in[k].copy_(hi, non_blocking=True)
-            in_ready[k].record(up)
-            comp.wait_event(in_ready[k])
-            if i >= 2:
-                comp.wait_event(out_free[k])           # the download of this output buffer is done
-            self(self._dev_in[k], chunk_stride, out=outs[k])
-            in_free[k].record(comp)
-            out_ready[k].record(comp)
-            down.wait_event(out_ready[k])
-            with torch.cuda.stream(down):
-                ho.copy_(outs[k], non_blocking=True)
-            out_free[k].record(down)
-        comp.wait_stream(down)
-        comp.wait_stream(up)
+        ds, pr = dims_struct(self.dims), precision_struct(self.precision)
+        layers = self.enc.layer_array(self.precision)
+        ln = _lib.wb_ln_weights(self.enc.ln_post_g.data_ptr(), self.enc.ln_post_b.data_ptr())
+        stem = self.stem.struct()
+        hp = _lib.wb_host_pipeline()
+        hp.dims, hp.batch, hp.samples_per_batch, hp.chunk_stride = ds, self.batch, host_in[0].numel(), chunk_stride
+        hp.stem, hp.layers, hp.ln_post, hp.precision = ctypes.pointer(stem), layers, ctypes.pointer(ln), pr
+        hp.dev_audio[0], hp.dev_audio[1] = self._dev_in[0].data_ptr(), self._dev_in[1].data_ptr()
+        hp.dev_mel, hp.dev_x0 = self.mel.data_ptr(), self.x0.data_ptr()
+        hp.dev_out[0], hp.dev_out[1] = self.out.data_ptr(), self._out2.data_ptr()
+        hp.ws_mel, hp.ws_mel_bytes = self.ws_mel.data_ptr(), self.ws_mel.numel()
+        hp.ws_stem, hp.ws_stem_bytes = self.ws_stem.data_ptr(), self.ws_stem.numel()
+        hp.ws_enc, hp.ws_enc_bytes = self.ws_enc.data_ptr(), self.ws_enc.numel()
+        if overlap:
+            hp.upload_stream, hp.download_stream = self._copy[0].cuda_stream, self._copy[1].cuda_stream
+        ins = (ctypes.c_void_p * n)(*[t.data_ptr() for t in host_in])
+        outs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in host_out])
+        call("wb_encode_host", ctypes.byref(hp), ins, outs, n, _stream())

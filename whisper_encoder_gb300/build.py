@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libwb.so")
-SOURCES = ["api.cu", "kernels.cu", "tc_kernels.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "kernels.cu", "tc_kernels.cu", "static_scratch.cu", "host_pipeline.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
