@@ -42,7 +42,8 @@ typedef enum {
   WB_ECUDA = -2,         /* a CUDA runtime/driver call or launch failed */
   WB_EUNSUPPORTED = -3,  /* valid request this build does not implement (e.g. mixed bf16 x E4M3 site) */
   WB_ETIMEOUT = -4,      /* a bounded device-side wait ran out (reported by wb_check_device_error) */
-  WB_EWORKSPACE = -5     /* workspace pointer null or smaller than the *_workspace_bytes() query */
+  WB_EWORKSPACE = -5,    /* workspace pointer null or smaller than the *_workspace_bytes() query */
+  WB_EBOUNDS = -6        /* debug builds only: a kernel index fell outside its buffer (wb_check_device_error) */
 } wb_status;
 
 /* Element types of one precision site (showcase site, "The Approach": a
@@ -114,10 +115,18 @@ const char* wb_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int wb_version(void);
 
-/* Synchronizes `stream`, then reads and clears this device's error word.
+/* 1 if this library was built with the debug bounds checks (-DWB_DEBUG), else 0.
+ * In a debug build every kernel load or store that does not go through a TMA
+ * tensor map checks its index against the extent of the buffer it addresses;
+ * an index outside is skipped and recorded in the device error word (bit 1,
+ * site in bits 8..15).  The arithmetic is otherwise the release build's. */
+int wb_debug_build(void);
+
+/* Synchronizes `stream`, then reads and clears this device's error words.
  * Returns WB_ETIMEOUT if any kernel recorded a bounded-wait timeout since the
- * last call, WB_ECUDA if the synchronization itself failed, else WB_OK.
- * *detail (optional) receives the raw word (bits 8..15: the wait site). */
+ * last call, else WB_EBOUNDS if a debug build's bounds check fired, WB_ECUDA
+ * if the synchronization itself failed, else WB_OK.  *detail (optional)
+ * receives the raw word (bit 0 timeout, bit 1 bounds, bits 8..15 the site). */
 wb_status wb_check_device_error(void* stream, uint32_t* detail);
 
 /* Wait site that wb_selftest_wait_timeout() records (bits 8..15 of the word). */

@@ -47,7 +47,7 @@ def test_header_constants_match_binding():
 def test_status_strings_and_version(lib):
     from whisper_encoder_gb300 import _lib
     assert lib.wb_version() >= 100
-    for code, word in [(0, "ok"), (-1, "invalid"), (-4, "timed out"), (-5, "workspace")]:
+    for code, word in [(0, "ok"), (-1, "invalid"), (-4, "timed out"), (-5, "workspace"), (-6, "bounds")]:
         assert word in _lib.status_string(code)
 
 

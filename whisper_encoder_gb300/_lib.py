@@ -13,7 +13,7 @@ from . import build as _build
 
 LIB_PATH = _build.LIB
 
-WB_OK, WB_EINVAL, WB_ECUDA, WB_EUNSUPPORTED, WB_ETIMEOUT, WB_EWORKSPACE = 0, -1, -2, -3, -4, -5
+WB_OK, WB_EINVAL, WB_ECUDA, WB_EUNSUPPORTED, WB_ETIMEOUT, WB_EWORKSPACE, WB_EBOUNDS = 0, -1, -2, -3, -4, -5, -6
 WB_BF16, WB_E4M3 = 0, 1
 WB_LOGMEL_STATIC_MAX_CHUNKS = 2   # include/wb.h
 WB_SELFTEST_WAIT_SITE = 0x7F      # include/wb.h
@@ -62,6 +62,7 @@ class wb_host_pipeline(ctypes.Structure):
 SIGNATURES = {
     "wb_status_string": (ctypes.c_char_p, [c_int]),
     "wb_version": (c_int, []),
+    "wb_debug_build": (c_int, []),
     "wb_check_device_error": (c_int, [c_void, P(ctypes.c_uint32)]),
     "wb_selftest_wait_timeout": (c_int, [c_void]),
     "wb_logmel_workspace_bytes": (c_size, [c_int, c_int]),
@@ -102,21 +103,25 @@ class WbError(RuntimeError):
         super().__init__(f"{fn} failed: {msg} ({status})")
 
 
-def load(path: str | None = None) -> ctypes.CDLL:
-    """Load libwb.so (built beforehand by whisper_encoder_gb300.build)."""
-    global _LIB
-    if _LIB is not None:
-        return _LIB
-    path = path or LIB_PATH
+def open_library(path: str) -> ctypes.CDLL:
+    """Open a build of libwb at ``path`` with the ctypes signatures of include/wb.h."""
     if not os.path.exists(path):
-        raise RuntimeError(f"libwb.so is not built ({path}); run `python -m whisper_encoder_gb300.build`")
+        raise RuntimeError(f"libwb is not built ({path}); run `python -m whisper_encoder_gb300.build`")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _LIB = lib
     return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libwb.so (built beforehand by whisper_encoder_gb300.build)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    _LIB = open_library(path or LIB_PATH)
+    return _LIB
 
 
 def status_string(status: int) -> str:

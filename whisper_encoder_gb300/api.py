@@ -280,13 +280,14 @@ def profile_end() -> dict:
 
 
 def check_device_error(stream=None) -> int:
-    """Synchronize, read and clear the device error word; 0 when no kernel reported a fault.
+    """Synchronize, read and clear the device error words; 0 when no kernel reported a fault.
 
-    A recorded timeout is returned as the raw word (bit 0 set, wait site in bits 8..15)
-    rather than raised; a failed synchronization raises WbError."""
+    A recorded timeout (bit 0) or, in a debug build, a failed bounds check (bit 1) is returned
+    as the raw word (site in bits 8..15) rather than raised; a failed synchronization raises
+    WbError."""
     word = ctypes.c_uint32(0)
     st = load().wb_check_device_error(_stream(stream), ctypes.byref(word))
-    if st not in (WB_OK, WB_ETIMEOUT):
+    if st not in (WB_OK, WB_ETIMEOUT, _lib.WB_EBOUNDS):
         raise WbError("wb_check_device_error", st)
     return word.value
 

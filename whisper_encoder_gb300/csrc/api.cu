@@ -210,6 +210,8 @@ wb_status dense_gemm(const void* A, const void* W, int M, int N, int K, bool fp8
   p.resid = static_cast<const __nv_bfloat16*>(resid);
   p.resid_ld = ldo;
   p.resid_item = static_cast<long long>(M) * ldo;
+  p.resid_elems = static_cast<long long>(M) * ldo;
+  p.amax_items = p.rows_per_item > 0 ? (M + p.rows_per_item - 1) / p.rows_per_item : 0;
   p.M = M;
   p.N = N;
   p.batch = 1;
@@ -329,25 +331,40 @@ const char* wb_status_string(int status) {
     case WB_EUNSUPPORTED: return "unsupported configuration";
     case WB_ETIMEOUT: return "device-side wait timed out";
     case WB_EWORKSPACE: return "workspace missing or too small";
+    case WB_EBOUNDS: return "a debug build's bounds check found an index outside its buffer";
     default: return "unknown status";
   }
 }
 
 int wb_version(void) { return 100; }
 
+int wb_debug_build(void) {
+#ifdef WB_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 wb_status wb_check_device_error(void* stream, uint32_t* detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return WB_ECUDA;
-  uint32_t* e = err_ptr();
-  if (!e) return WB_ECUDA;
+  // the tensor-core kernels' word and the SIMT kernels' word (bounds checks of debug builds)
+  uint32_t* words[2] = {err_ptr(), simt_err_ptr()};
   uint32_t word = 0;
-  if (cudaMemcpy(&word, e, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return WB_ECUDA;
-  if (word) {
-    const uint32_t zero = 0;
-    if (cudaMemcpy(e, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return WB_ECUDA;
+  for (uint32_t* e : words) {
+    if (!e) return WB_ECUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, e, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return WB_ECUDA;
+    if (w) {
+      const uint32_t zero = 0;
+      if (cudaMemcpy(e, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return WB_ECUDA;
+    }
+    word |= w;
   }
   if (detail) *detail = word;
-  return (word & ERR_TIMEOUT) ? WB_ETIMEOUT : WB_OK;
+  if (word & ERR_TIMEOUT) return WB_ETIMEOUT;
+  return (word & ERR_BOUNDS) ? WB_EBOUNDS : WB_OK;
 }
 
 wb_status wb_selftest_wait_timeout(void* stream) {
@@ -417,6 +434,7 @@ wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride,
     p.n_pass = np;
     p.pw = pw;
     p.pw_ld = N_BIN_PAD;
+    p.pw_elems = static_cast<long long>(n_chunks) * 2 * N_FRAMES * N_BIN_PAD;
     g.p = p;
     Prof pr(PC_LOGMEL_DFT, s);
     WB_CUDA(launch_gemm(g, s));
@@ -447,6 +465,7 @@ wb_status wb_logmel(const float* audio, int64_t n_samples, int64_t chunk_stride,
     p.mel_out = out;
     p.mel_max = mmax;
     p.n_valid = n_mels;
+    p.mel_elems = static_cast<long long>(n_chunks) * n_mels * N_FRAMES;
     g.p = p;
     Prof pr(PC_LOGMEL_MEL, s);
     WB_CUDA(launch_gemm(g, s));
@@ -642,6 +661,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
       p.vt_col0 = 2 * D;
       p.vt_T = T_TOK;
       p.vt_ld = T_PAD;
+      p.vt_elems = static_cast<long long>(batch) * H * 64 * T_PAD;
       if (q8) {
         p.amax_a = am_qkv;
         p.scale_b = W.s_qkv;

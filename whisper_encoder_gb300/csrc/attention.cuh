@@ -341,11 +341,12 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t wa = pack_bf16(__uint_as_float(v[4 * kk]) * ia, __uint_as_float(v[4 * kk + 1]) * ia);
         const uint32_t wb = pack_bf16(__uint_as_float(v[4 * kk + 2]) * ib, __uint_as_float(v[4 * kk + 3]) * ib);
-        if (qa < p.T) {
+        const long long out_el = static_cast<long long>(p.batch) * p.T * p.d;
+        if (qa < p.T && in_bounds(p.err, (oa + 8 * kk) - p.out, 2, out_el, SITE_ATT_OUT)) {
           *reinterpret_cast<uint32_t*>(oa + 8 * kk) = wa;
           mx2 = bf16x2_max(mx2, wa & 0x7fff7fffu);
         }
-        if (qb < p.T) {
+        if (qb < p.T && in_bounds(p.err, (ob + 8 * kk) - p.out, 2, out_el, SITE_ATT_OUT)) {
           *reinterpret_cast<uint32_t*>(ob + 8 * kk) = wb;
           mx2 = bf16x2_max(mx2, wb & 0x7fff7fffu);
         }
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(ATT_THREADS, ATT_CTAS_PER_SM)
         float mx = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xffff0000u));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0 && mx > 0.0f) atomic_max_nonneg(p.amax + b, mx);
+        if (lane == 0 && mx > 0.0f && in_bounds(p.err, b, 1, p.batch, SITE_ATT_AMAX)) atomic_max_nonneg(p.amax + b, mx);
       }
     }
   }

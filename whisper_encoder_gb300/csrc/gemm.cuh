@@ -209,9 +209,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int n0 = ncol0 + c * 32;
 #pragma unroll
           for (int j = 0; j < 4; ++j) rres[4 * c + j] = make_uint4(0u, 0u, 0u, 0u);
-          if (row_ok && n0 < p.N) {
-            const uint4* rp = reinterpret_cast<const uint4*>(
-                p.resid + b * p.resid_item + static_cast<long long>(p.out_row_off + m) * p.resid_ld + n0);
+          const long long ri = b * p.resid_item + static_cast<long long>(p.out_row_off + m) * p.resid_ld + n0;
+          if (row_ok && n0 < p.N && in_bounds(p.err, ri, 32, p.resid_elems, SITE_GEMM_RESID)) {
+            const uint4* rp = reinterpret_cast<const uint4*>(p.resid + ri);
 #pragma unroll
             for (int j = 0; j < 4; ++j) rres[4 * c + j] = rp[j];
           }
@@ -220,7 +220,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // folded LayerNorm: this row's (mean, rstd), fetched while the accumulator is still being computed
       const bool lnf = (EPI == EPI_BIAS || EPI == EPI_BIAS_GELU) && !FP8 && p.ln_stats != nullptr;
       float2 ln_mr = make_float2(0.0f, 1.0f);
-      if (lnf && row_ok) ln_mr = p.ln_stats[static_cast<long long>(b) * p.M + m];
+      if (lnf && row_ok &&
+          in_bounds(p.err, static_cast<long long>(b) * p.M + m, 1, static_cast<long long>(p.batch) * p.M,
+                    SITE_GEMM_LNSTATS))
+        ln_mr = p.ln_stats[static_cast<long long>(b) * p.M + m];
       if (!mbar_wait(&tfull[acc], acc_phase, p.err, abort_flag, 4)) { ok = false; break; }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int item = p.rows_per_item > 0 ? (b * p.M + (row_ok ? m : p.M - 1)) / p.rows_per_item : 0;
         float alpha = alpha_w * alpha_a;
         if (FP8 && p.amax_a) {
-          const float am = __ldg(p.amax_a + item);
+          const float am = in_bounds(p.err, item, 1, p.amax_items, SITE_GEMM_AMAX) ? __ldg(p.amax_a + item) : 0.0f;
           alpha = alpha_w * (am > 0.0f ? am / 448.0f : 1.0f);
         }
         float tile_amax = 0.0f;
@@ -247,6 +250,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (lane == 0) mbar_arrive(&tempty[acc]);     // accumulator is free for tile i+2
           }
           if (n0 >= p.N) continue;
+          if (!in_bounds(p.err, n0, 32, p.N, SITE_GEMM_BIAS)) continue;
 
           // bias (+ E4M3 scale) and activation
           const float4* bp = reinterpret_cast<const float4*>(p.bias + n0);
@@ -284,8 +288,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
               if (EPI == EPI_CONV2) {   // positional embedding from the table (row m, this column pair)
                 const int mr = row_ok ? m : p.M - 1;      // rows past M are not stored; stay inside the table
-                const float2 pe = __ldg(reinterpret_cast<const float2*>(p.pos + static_cast<long long>(mr) * p.N + n0 +
-                                                                        4 * i4 + kk));
+                const long long pi = static_cast<long long>(mr) * p.N + n0 + 4 * i4 + kk;
+                const float2 pe = in_bounds(p.err, pi, 2, static_cast<long long>(p.M) * p.N, SITE_GEMM_POS)
+                                      ? __ldg(reinterpret_cast<const float2*>(p.pos + pi))
+                                      : make_float2(0.0f, 0.0f);
                 x0 += pe.x;
                 x1 += pe.y;
               }
@@ -300,10 +306,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const int gb = m / p.vt_T, t = m % p.vt_T;
               const int h = col >> 6, e0 = col & 63;
               const int H = (p.N - p.vt_col0) >> 6;
-              __half* dst = p.vt + (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
+              const long long di = (static_cast<long long>(gb * H + h) * 64 + e0) * p.vt_ld + t;
+              __half* dst = p.vt + di;
+              if (in_bounds(p.err, di, 31LL * p.vt_ld + 1, p.vt_elems, SITE_GEMM_VT)) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)   // f16 for the attention's f16 P.V product (saturated to its range)
-                dst[static_cast<long long>(i) * p.vt_ld] = __float2half_rn(fminf(fmaxf(v[i], -65504.0f), 65504.0f));
+                for (int i = 0; i < 32; ++i)   // f16 for the attention's f16 P.V product (saturated to its range)
+                  dst[static_cast<long long>(i) * p.vt_ld] = __float2half_rn(fminf(fmaxf(v[i], -65504.0f), 65504.0f));
+              }
             }
             continue;
           }
@@ -341,8 +350,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (__all_sync(0xffffffffu, item == item0)) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) tile_amax = fmaxf(tile_amax, __shfl_xor_sync(0xffffffffu, tile_amax, o));
-            if (lane == 0 && tile_amax > 0.0f) atomic_max_nonneg(p.amax + item0, tile_amax);
-          } else if (tile_amax > 0.0f) {
+            if (lane == 0 && tile_amax > 0.0f && in_bounds(p.err, item0, 1, p.amax_items, SITE_GEMM_AMAX))
+              atomic_max_nonneg(p.amax + item0, tile_amax);
+          } else if (tile_amax > 0.0f && in_bounds(p.err, item, 1, p.amax_items, SITE_GEMM_AMAX)) {
             atomic_max_nonneg(p.amax + item, tile_amax);
           }
         }
@@ -355,7 +365,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-        if (row_ok) {
+        const long long rowi_c = static_cast<long long>(b) * 2 * p.M + m;
+        if (row_ok && in_bounds(p.err, (rowi_c + p.M) * p.pw_ld + nt * (BN / 2) + cg * 32, 32, p.pw_elems,
+                                SITE_GEMM_POWER)) {
           const int bin0 = nt * (BN / 2) + cg * 32;
           uint4 hi[4], lo[4];
           uint32_t* h32 = reinterpret_cast<uint32_t*>(hi);
@@ -386,7 +398,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) mbar_arrive(&tempty[acc]);
         const int n0 = nt * BN + cg * 32;
         float local_max = 0.0f;
-        if (row_ok && n0 < p.n_valid) {
+        const int n_hi = (p.n_valid - n0 < 32 ? p.n_valid - n0 : 32) - 1;   // last bin this warp writes
+        if (row_ok && n0 < p.n_valid &&
+            in_bounds(p.err, (static_cast<long long>(b) * p.n_valid + n0 + n_hi) * p.M + m, 1, p.mel_elems,
+                      SITE_GEMM_MEL)) {
           float* dst = p.mel_out + (static_cast<long long>(b) * p.n_valid + n0) * p.M + m;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -399,7 +414,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) local_max = fmaxf(local_max, __shfl_xor_sync(0xffffffffu, local_max, o));
-        if (lane == 0 && local_max > 0.0f) atomic_max_nonneg(p.mel_max + b, local_max);
+        if (lane == 0 && local_max > 0.0f && in_bounds(p.err, b, 1, p.batch, SITE_GEMM_MEL))
+          atomic_max_nonneg(p.mel_max + b, local_max);
       }
     }
 

@@ -3,12 +3,20 @@
 // fused residual + LayerNorm, FP8 absmax / quantise / dequantise.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace wb {
 
+// Error word of the bounds checks that debug builds compile into this file's kernels (read and
+// cleared by wb_check_device_error through simt_err_ptr()).
+__device__ uint32_t g_simt_err;
+
 namespace {
+
+#define WB_IN(idx, len, extent, site) in_bounds(&g_simt_err, (idx), (len), (extent), (site))
 
 constexpr int EW_THREADS = 256;
 
@@ -40,10 +48,11 @@ __global__ void pad_split_kernel(const float* __restrict__ audio, long long n_sa
     const float r1 = x - __bfloat162float(a);
     const __nv_bfloat16 b = __float2bfloat16_rn(r1);
     const __nv_bfloat16 e = __float2bfloat16_rn(r1 - __bfloat162float(b));
-    __nv_bfloat16* base = xs + static_cast<long long>(c) * 3 * PADDED;
-    base[j] = a;
-    base[PADDED + j] = b;
-    base[2 * PADDED + j] = e;
+    const long long o = static_cast<long long>(c) * 3 * PADDED + j;
+    if (!WB_IN(o, 2 * PADDED + 1, static_cast<long long>(n_chunks) * 3 * PADDED, SITE_PAD_SPLIT)) continue;
+    xs[o] = a;
+    xs[o + PADDED] = b;
+    xs[o + 2 * PADDED] = e;
   }
 }
 
@@ -70,6 +79,7 @@ __global__ void dft_basis_kernel(__nv_bfloat16* __restrict__ basis) {
   const float r1 = v - __bfloat162float(a);
   const __nv_bfloat16 b = __float2bfloat16_rn(r1);
   const __nv_bfloat16 e = __float2bfloat16_rn(r1 - __bfloat162float(b));
+  if (!WB_IN((2 * DFT_ROWS + row) * N_FFT + k, 1, 3 * DFT_ROWS * N_FFT, SITE_DFT_BASIS)) return;
   basis[(0 * DFT_ROWS + row) * N_FFT + k] = a;
   basis[(1 * DFT_ROWS + row) * N_FFT + k] = b;
   basis[(2 * DFT_ROWS + row) * N_FFT + k] = e;
@@ -100,6 +110,7 @@ __global__ void mel_fb_kernel(__nv_bfloat16* __restrict__ fbs, int n_mels) {
   }
   const __nv_bfloat16 a = __float2bfloat16_rn(v);
   const __nv_bfloat16 b = __float2bfloat16_rn(v - __bfloat162float(a));
+  if (!WB_IN((MEL_ROWS + m) * N_BIN_PAD + k, 1, 2 * MEL_ROWS * N_BIN_PAD, SITE_MEL_FB)) return;
   fbs[m * N_BIN_PAD + k] = a;
   fbs[(MEL_ROWS + m) * N_BIN_PAD + k] = b;
 }
@@ -111,6 +122,9 @@ __global__ void logmel_post_kernel(float* __restrict__ out, const float* __restr
   float4* p = reinterpret_cast<float4*>(out + static_cast<long long>(b) * per_chunk);
   const int n4 = per_chunk / 4;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
+    if (!WB_IN(static_cast<long long>(b) * per_chunk + 4LL * i, 4, static_cast<long long>(gridDim.y) * per_chunk,
+               SITE_LOGMEL_POST))
+      continue;
     float4 v = p[i];
     v.x = (fmaxf(v.x, thr) + 4.0f) * 0.25f;
     v.y = (fmaxf(v.y, thr) + 4.0f) * 0.25f;
@@ -126,13 +140,18 @@ __global__ void stem_transpose_kernel(const float* __restrict__ in, int C, __nv_
   const int b = blockIdx.z, t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
   for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
     const int c = c0 + ty, t = t0 + threadIdx.x;
-    tile[ty][threadIdx.x] = (c < C && t < N_FRAMES) ? in[(static_cast<long long>(b) * C + c) * N_FRAMES + t] : 0.0f;
+    const long long ii = (static_cast<long long>(b) * C + c) * N_FRAMES + t;
+    tile[ty][threadIdx.x] = (c < C && t < N_FRAMES && WB_IN(ii, 1, static_cast<long long>(gridDim.z) * C * N_FRAMES,
+                                                           SITE_STEM_T_IN))
+                                ? in[ii]
+                                : 0.0f;
   }
   __syncthreads();
   for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
     const int t = t0 + ty, c = c0 + threadIdx.x;
-    if (t < N_FRAMES && c < C)
-      out[(static_cast<long long>(b) * (N_FRAMES + 2) + 1 + t) * C + c] = __float2bfloat16_rn(tile[threadIdx.x][ty]);
+    const long long oi = (static_cast<long long>(b) * (N_FRAMES + 2) + 1 + t) * C + c;
+    if (t < N_FRAMES && c < C && WB_IN(oi, 1, static_cast<long long>(gridDim.z) * (N_FRAMES + 2) * C, SITE_STEM_T_OUT))
+      out[oi] = __float2bfloat16_rn(tile[threadIdx.x][ty]);
   }
 }
 
@@ -142,7 +161,8 @@ __global__ void zero_rows_kernel(__nv_bfloat16* base, long long row_elems, long 
   if (b >= batch) return;
   __nv_bfloat16* p = base + b * batch_stride + row * row_elems;
   for (long long i = blockIdx.x * blockDim.x + threadIdx.x; i < row_elems; i += gridDim.x * blockDim.x)
-    p[i] = __float2bfloat16_rn(0.0f);
+    if (WB_IN(b * batch_stride + row * row_elems + i, 1, batch * batch_stride, SITE_ZERO_ROWS))
+      p[i] = __float2bfloat16_rn(0.0f);
 }
 
 // PyTorch Conv1d weight [c_out][c_in][3] float32 -> tap-major bf16 [3][c_out][c_in].
@@ -152,7 +172,8 @@ __global__ void pack_conv_kernel(const float* __restrict__ w, int c_out, int c_i
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int j = static_cast<int>(i % 3);
     const long long oi = i / 3;   // o * c_in + ci
-    out[j * static_cast<long long>(c_out) * c_in + oi] = __float2bfloat16_rn(w[i]);
+    if (WB_IN(j * static_cast<long long>(c_out) * c_in + oi, 1, n, SITE_PACK_CONV))
+      out[j * static_cast<long long>(c_out) * c_in + oi] = __float2bfloat16_rn(w[i]);
   }
 }
 
@@ -175,12 +196,13 @@ constexpr int LN_WARPS = 8;
 
 template <int NV, int VEC, bool RES>
 __device__ __forceinline__ void ln_load(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ res,
-                                        long long row, int lane, typename VecIO<VEC>::T (&u)[NV],
+                                        long long row, long long rows, int lane, typename VecIO<VEC>::T (&u)[NV],
                                         typename VecIO<VEC>::T (&ur)[NV]) {
   using V = typename VecIO<VEC>::T;
   constexpr int D = NV * VEC * 32;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
+    if (!WB_IN(row * D + (i * 32 + lane) * VEC, VEC, rows * D, SITE_LN_X)) continue;
     u[i] = __ldg(reinterpret_cast<const V*>(x + row * D + (i * 32 + lane) * VEC));
     if (RES) ur[i] = __ldg(reinterpret_cast<const V*>(res + row * D + (i * 32 + lane) * VEC));
   }
@@ -202,9 +224,9 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   const long long r0 = warp_g * per;
   const long long r1 = r0 + per < rows ? r0 + per : rows;
   V u[NV], ur[NV], nu[NV], nur[NV];
-  if (r0 < r1) ln_load<NV, VEC, RES>(x, res, r0, lane, u, ur);
+  if (r0 < r1) ln_load<NV, VEC, RES>(x, res, r0, rows, lane, u, ur);
   for (long long row = r0; row < r1; ++row) {
-    if (row + 1 < r1) ln_load<NV, VEC, RES>(x, res, row + 1, lane, nu, nur);
+    if (row + 1 < r1) ln_load<NV, VEC, RES>(x, res, row + 1, rows, lane, nu, nur);
     float v[NV * VEC];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -220,7 +242,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
           uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
           for (int j = 0; j < VEC / 2; ++j) o32[j] = pack_bf16(v[i * VEC + 2 * j], v[i * VEC + 2 * j + 1]);
-          *reinterpret_cast<V*>(total + row * D + (i * 32 + lane) * VEC) = o;
+          if (WB_IN(row * D + (i * 32 + lane) * VEC, VEC, static_cast<long long>(rows) * D, SITE_LN_Y))
+            *reinterpret_cast<V*>(total + row * D + (i * 32 + lane) * VEC) = o;
         }
       }
     }
@@ -245,6 +268,7 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int off = (i * 32 + lane) * VEC;
+      if (!WB_IN(off, VEC, D, SITE_LN_GB)) continue;
       // gamma / beta for this lane's VEC columns as 16-byte vector loads (L1-resident, coalesced)
       float gg[VEC], bb[VEC];
 #pragma unroll
@@ -262,7 +286,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
         const float y1 = fmaf((v[i * VEC + 2 * j + 1] - mean) * rstd, gg[2 * j + 1], bb[2 * j + 1]);
         o32[j] = pack_bf16(y0, y1);
       }
-      *reinterpret_cast<V*>(y + row * D + off) = o;
+      if (WB_IN(row * D + off, VEC, static_cast<long long>(rows) * D, SITE_LN_Y))
+        *reinterpret_cast<V*>(y + row * D + off) = o;
     }
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -316,8 +341,11 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
   const long long r1 = r0 + per < rows ? r0 + per : rows;
   auto load = [&](long long row, uint2 (&u)[NK]) {
 #pragma unroll
-    for (int k = 0; k < NK; ++k) u[k] = __ldg(reinterpret_cast<const uint2*>(x + row * D + 128 * k) + lane);
+    for (int k = 0; k < NK; ++k)
+      if (WB_IN(row * D + 128 * k + 4 * lane, 4, static_cast<long long>(rows) * D, SITE_STATS_X))
+        u[k] = __ldg(reinterpret_cast<const uint2*>(x + row * D + 128 * k) + lane);
   };
+  const int n_items = (rows + rows_per_item - 1) / rows_per_item;
   uint2 u[NK], nu[NK];
   if (r0 < r1) load(r0, u);
   uint32_t run_max2 = 0u;                          // packed bf16 |y| maxima of the current item
@@ -326,7 +354,7 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
     float m = fmaxf(__uint_as_float(run_max2 << 16), __uint_as_float(run_max2 & 0xffff0000u));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0 && m > 0.0f) atomic_max_nonneg(amax + run_item, m);
+    if (lane == 0 && m > 0.0f && WB_IN(run_item, 1, n_items, SITE_STATS_AMAX)) atomic_max_nonneg(amax + run_item, m);
   };
   for (long long row = r0; row < r1; ++row) {
     if (row + 1 < r1) load(row + 1, nu);
@@ -349,7 +377,7 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
     const float rstd = rsqrtf(q * (1.0f / D) + eps);
-    if (lane == 0) stats[row] = make_float2(mean, rstd);
+    if (lane == 0 && WB_IN(row, 1, rows, SITE_STATS_OUT)) stats[row] = make_float2(mean, rstd);
     if (!AMAX) {
 #pragma unroll
       for (int k = 0; k < NK; ++k) u[k] = nu[k];
@@ -392,6 +420,7 @@ __global__ void __launch_bounds__(256)
   grid_dependents_launch();
   const int t = threadIdx.x;
   if (8 * t >= d) return;
+  const int n_items = (rows + rows_per_item - 1) / rows_per_item;
   const float4 ga = __ldg(reinterpret_cast<const float4*>(g) + 2 * t), gb = __ldg(reinterpret_cast<const float4*>(g) + 2 * t + 1);
   const float4 ba = __ldg(reinterpret_cast<const float4*>(bta) + 2 * t), bb = __ldg(reinterpret_cast<const float4*>(bta) + 2 * t + 1);
   const uint64_t g2[4] = {f32x2_pack(ga.x, ga.y), f32x2_pack(ga.z, ga.w), f32x2_pack(gb.x, gb.y), f32x2_pack(gb.z, gb.w)};
@@ -400,7 +429,7 @@ __global__ void __launch_bounds__(256)
   int item = row0 / rows_per_item;                 // items advance at most once every rows_per_item rows
   int item_end = (item + 1) * rows_per_item;
   float inv = 1.0f;
-  {
+  if (WB_IN(item, 1, n_items, SITE_LNQ_AUX)) {
     const float a = __ldg(amax + item);
     inv = a > 0.0f ? 448.0f / a : 1.0f;
   }
@@ -410,8 +439,10 @@ __global__ void __launch_bounds__(256)
     uint4 u[LNQ_RG];
 #pragma unroll
     for (int r = 0; r < LNQ_RG; ++r)
-      u[r] = rb + r < rows ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(rb + r) * d) + t)
-                           : make_uint4(0u, 0u, 0u, 0u);
+      u[r] = rb + r < rows && WB_IN(static_cast<long long>(rb + r) * d + 8 * t, 8, static_cast<long long>(rows) * d,
+                                    SITE_LNQ_X)
+                 ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(rb + r) * d) + t)
+                 : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int r = 0; r < LNQ_RG; ++r) {
       const int row = rb + r;
@@ -419,10 +450,10 @@ __global__ void __launch_bounds__(256)
       while (row >= item_end) {
         ++item;
         item_end += rows_per_item;
-        const float a = __ldg(amax + item);
+        const float a = WB_IN(item, 1, n_items, SITE_LNQ_AUX) ? __ldg(amax + item) : 0.0f;
         inv = a > 0.0f ? 448.0f / a : 1.0f;
       }
-      const float2 st = __ldg(stats + row);
+      const float2 st = WB_IN(row, 1, rows, SITE_LNQ_AUX) ? __ldg(stats + row) : make_float2(0.0f, 1.0f);
       const uint64_t nm2 = f32x2_pack(-st.x, -st.x), rs2 = f32x2_pack(st.y, st.y), inv2 = f32x2_pack(inv, inv);
       const uint32_t w[4] = {u[r].x, u[r].y, u[r].z, u[r].w};
       uint32_t c[2];
@@ -435,7 +466,8 @@ __global__ void __launch_bounds__(256)
                                                                             g2[2 * k + 1], b2[2 * k + 1]))), inv2), s2, s3);
         c[k] = static_cast<uint32_t>(cvt_e4m3x2(s0, s1)) | (static_cast<uint32_t>(cvt_e4m3x2(s2, s3)) << 16);
       }
-      reinterpret_cast<uint2*>(q + static_cast<long long>(row) * d)[t] = make_uint2(c[0], c[1]);
+      if (WB_IN(static_cast<long long>(row) * d + 8 * t, 8, static_cast<long long>(rows) * d, SITE_LNQ_Q))
+        reinterpret_cast<uint2*>(q + static_cast<long long>(row) * d)[t] = make_uint2(c[0], c[1]);
     }
   }
 }
@@ -462,7 +494,7 @@ __global__ void ln_row_stats_kernel(const __nv_bfloat16* __restrict__ x, long lo
     float s1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < STATS_MAXC; ++i) {
-      if (lane + 32 * i < nc) {
+      if (lane + 32 * i < nc && WB_IN(row * d + 8LL * (lane + 32 * i), 8, rows * d, SITE_ROWSTATS)) {
         u[i] = src[lane + 32 * i];
         const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u[i]);
 #pragma unroll
@@ -486,7 +518,8 @@ __global__ void ln_row_stats_kernel(const __nv_bfloat16* __restrict__ x, long lo
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-    if (lane == 0) out[row] = make_float2(mean, rsqrtf(q / static_cast<float>(d) + eps));
+    if (lane == 0 && WB_IN(row, 1, rows, SITE_ROWSTATS))
+      out[row] = make_float2(mean, rsqrtf(q / static_cast<float>(d) + eps));
   }
 }
 
@@ -502,6 +535,7 @@ __global__ void fold_ln_kernel(const __nv_bfloat16* __restrict__ w, const float*
   __nv_bfloat16* orow = w_ln + n * d;
   float sc = 0.0f, sb = 0.0f;
   for (int k = lane; k < d; k += 32) {
+    if (!WB_IN(n * d + k, 1, static_cast<long long>(n_out) * d, SITE_FOLD)) continue;
     const float wv = __bfloat162float(wr[k]);
     const __nv_bfloat16 f = __float2bfloat16_rn(wv * gamma[k]);
     orow[k] = f;
@@ -528,6 +562,7 @@ __global__ void amax_kernel(const __nv_bfloat16* __restrict__ x, long long n, fl
   const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = tid; i < n8; i += step) {
+    if (!WB_IN(8 * i, 8, n, SITE_AMAX)) continue;
     uint4 u = reinterpret_cast<const uint4*>(x)[i];
     const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
 #pragma unroll
@@ -557,6 +592,7 @@ __global__ void quantize_kernel(const __nv_bfloat16* __restrict__ x, long long n
   const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = tid; i < n16; i += step) {
+    if (!WB_IN(16 * i, 16, n, SITE_QUANT)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * i;
     uint4 u0 = src[0], u1 = src[1];
     const __nv_bfloat16* h0 = reinterpret_cast<const __nv_bfloat16*>(&u0);
@@ -581,8 +617,10 @@ __global__ void quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, long l
   const long long n16 = n / 16;
   const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long n_items = (n / cols + rows_per_item - 1) / rows_per_item;
   for (long long i = tid; i < n16; i += step) {
     const int item = static_cast<int>((i * 16) / cols / rows_per_item);
+    if (!WB_IN(16 * i, 16, n, SITE_QUANT_ROWS) || !WB_IN(item, 1, n_items, SITE_QUANT_ROWS)) continue;
     const float a = __ldg(amax + item);
     const float inv = a > 0.0f ? 448.0f / a : 1.0f;
     const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * i;
@@ -657,14 +695,18 @@ __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, long lon
   const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;  // c over H*64 columns
   for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
     const int t = t0 + ty;
-    tile[ty][threadIdx.x] =
-        t < T ? v[(static_cast<long long>(b) * T + t) * ld + c0 + threadIdx.x] : __float2bfloat16_rn(0.0f);
+    const long long vi = (static_cast<long long>(b) * T + t) * ld + c0 + threadIdx.x;
+    tile[ty][threadIdx.x] = t < T && WB_IN(vi, 1, static_cast<long long>(gridDim.z) * T * ld, SITE_TRANSPOSE_V_IN)
+                                ? v[vi]
+                                : __float2bfloat16_rn(0.0f);
   }
   __syncthreads();
   for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
     const int c = c0 + ty, t = t0 + threadIdx.x;
     const int h = c >> 6, e = c & 63;
-    if (t < T) vt[(static_cast<long long>(b * H + h) * 64 + e) * T_PAD + t] = __float2half_rn(__bfloat162float(tile[threadIdx.x][ty]));
+    const long long oi = (static_cast<long long>(b * H + h) * 64 + e) * T_PAD + t;
+    if (t < T && WB_IN(oi, 1, static_cast<long long>(gridDim.z) * H * 64 * T_PAD, SITE_TRANSPOSE_V_OUT))
+      vt[oi] = __float2half_rn(__bfloat162float(tile[threadIdx.x][ty]));
   }
 }
 
@@ -933,6 +975,21 @@ __global__ void wait_timeout_selftest_kernel(uint32_t* err, uint32_t site) {
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint32_t site, cudaStream_t s) {
   wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err, site);
   return cudaGetLastError();
+}
+
+uint32_t* simt_err_ptr() {
+  constexpr int kMaxDev = 64;
+  static uint32_t* ptrs[kMaxDev] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_simt_err) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
 }
 
 }  // namespace wb

@@ -21,6 +21,28 @@ namespace wb {
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint32_t WAIT_ITER_LIMIT = 1u << 30;
 
+// ---------------------------------------------------------------------------
+// Debug builds (compiled with -DWB_DEBUG): every plain global load and store of
+// the kernels (the accesses that do not go through a TMA tensor map, whose
+// hardware clips boxes to the tensor) checks that the elements [idx, idx + len)
+// it touches lie inside [0, extent) of the buffer it addresses.  An access
+// outside is skipped and recorded in the error word as ERR_BOUNDS | site << 8.
+// Release builds compile the checks away.
+// ---------------------------------------------------------------------------
+#ifdef WB_DEBUG
+constexpr bool kBoundsChecks = true;
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(uint32_t* err, long long idx, long long len, long long extent,
+                                          uint32_t site) {
+  if (!kBoundsChecks) return true;
+  if (idx >= 0 && len >= 0 && idx + len <= extent) return true;
+  if (err) atomicOr(err, ERR_BOUNDS | (site << 8));
+  return false;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -68,6 +68,10 @@ struct GemmParams {
   float* mel_max;            // [batch] max of the mel power (bit pattern, >= 0)
   int n_valid;
   uint32_t* err;
+  // extents (elements) of the buffers the epilogue reaches with plain loads and stores, for the
+  // bounds checks of debug builds (unused otherwise)
+  long long resid_elems, vt_elems, pw_elems, mel_elems;
+  int amax_items;            // entries of amax / amax_a
 };
 
 constexpr int ATT_BQ = 128;           // queries per CTA
@@ -104,6 +108,18 @@ struct AttnParams {
   __nv_bfloat16* out;  // [batch * T, d]
   float* amax;         // if set: amax[b] = max |bf16 output| over batch item b (atomic; for an E4M3 scale)
   uint32_t* err;
+};
+
+// Sites (bits 8..15 of the error word) of the debug bounds checks: 0x20-0x3F the SIMT kernels,
+// 0x40-0x4F the GEMM epilogues, 0x50-0x5F the attention epilogue.
+enum : uint32_t {
+  SITE_PAD_SPLIT = 0x20, SITE_DFT_BASIS, SITE_MEL_FB, SITE_LOGMEL_POST, SITE_STEM_T_IN, SITE_STEM_T_OUT,
+  SITE_ZERO_ROWS, SITE_PACK_CONV, SITE_LN_X, SITE_LN_Y, SITE_LN_GB, SITE_STATS_X, SITE_STATS_OUT,
+  SITE_STATS_AMAX, SITE_LNQ_X, SITE_LNQ_Q, SITE_LNQ_AUX, SITE_ROWSTATS, SITE_FOLD, SITE_QUANT,
+  SITE_QUANT_ROWS, SITE_E5M2, SITE_DEQUANT, SITE_TRANSPOSE_V_IN, SITE_TRANSPOSE_V_OUT, SITE_POS, SITE_AMAX,
+  SITE_GEMM_RESID = 0x40, SITE_GEMM_BIAS, SITE_GEMM_LNSTATS, SITE_GEMM_POS, SITE_GEMM_VT, SITE_GEMM_POWER,
+  SITE_GEMM_MEL, SITE_GEMM_AMAX,
+  SITE_ATT_OUT = 0x50, SITE_ATT_AMAX
 };
 
 }  // namespace wb
