@@ -175,6 +175,15 @@ def test_large_v3_batch32_mixed_fp8(wb, batch32):
     # measured 6.45e-2 and 8.10e-2 on the code this bound was set on; a regression of more than
     # about 10 % fails
     assert e2e8 < 7e-2 and e2e < 9e-2
+    # the float64 E4M3 oracle drifts from itself by this much when only its residual stream is stored
+    # as bf16 between layers (tests/golden/fp8_drift.json, written from the oracle alone): a bf16
+    # pipeline's distance from the E4M3 oracle is of that size, not a sign of a wrong decision
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "fp8_drift.json")) as fh:
+        own = json.load(fh)["final_ln"]["e4m3_b_vs_e4m3"]
+    print(f"mixed_fp8: E4M3 oracle with bf16 residual storage vs E4M3 oracle {own:.3e}")
+    assert e2e8 < 1.2 * own
     pipe1 = wb.Pipeline(DIMS, stem, enc, batch=1, precision=wb.PRESET_MIXED_FP8)
     for b in (0, 17, 31):
         assert torch.equal(pipe1(_dev(audio[b]))[0], out[b]), b

@@ -35,3 +35,38 @@ def test_quantisation_alone_exceeds_6e2_within_five_layers():
     assert all(b > a for a, b in zip(gap, gap[1:]))           # the gap accumulates layer by layer
     assert gap[0] > 3e-2                                      # one layer already takes half the budget
     assert gap[-1] > 6e-2                                     # five layers exceed it
+
+
+def _drift():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "fp8_drift.json")) as fh:
+        return json.load(fh)
+
+
+def test_stored_drift_comes_from_this_oracle():
+    # tests/golden/fp8_drift.json is written by tests/golden/make_fp8_drift.py (oracle only, ~25 min);
+    # its first layer is recomputed here, so a change of the oracle's arithmetic shows up as a mismatch
+    from oracle import fp8 as ofp8
+    d = _drift()
+    assert len(d["per_layer"]) == 32
+    dims = synthetic.LARGE_V3
+    w = synthetic.encoder_weights(dims, d["workload"]["weights_seed"], "bf16", n_layers=1)
+    x0 = oenc.conv_stem(ofe.log_mel(synthetic.tone_chunk(d["workload"]["chunk_seed"]), dims.n_mels), w)
+    L = w["layers"][0]
+    plain = oenc.encoder_layer(x0, L, dims.n_heads)
+    q = oenc.encoder_layer(x0, L, dims.n_heads, oenc.MIXED_FP8)
+    qb = ofp8.round_bf16(q)
+    rel = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))  # noqa: E731
+    assert abs(rel(q, plain) - d["per_layer"][0]["e4m3_vs_plain"]) < 1e-12
+    assert abs(rel(qb, q) - d["per_layer"][0]["e4m3_b_vs_e4m3"]) < 1e-12
+
+
+def test_stored_drift_shape():
+    # both gaps grow with depth; bf16 storage of the residual stream alone, amplified by the E4M3
+    # decisions downstream of it, moves the E4M3 oracle by several 1e-2 over the 32 layers
+    d = _drift()
+    e, b = [r["e4m3_vs_plain"] for r in d["per_layer"]], [r["e4m3_b_vs_e4m3"] for r in d["per_layer"]]
+    assert b[0] < 2e-3 < 1e-2 < b[1]                      # one bf16 rounding, then the first E4M3 layer after it
+    assert max(b[-4:]) > 4e-2 and e[-1] > 6e-2
+    assert d["final_ln"]["e4m3_vs_plain"] > 6e-2
