@@ -279,12 +279,19 @@ def run_case(args) -> None:
     def rnd(*shape, scale=1.0):
         return (torch.randn(*shape, device="cuda", generator=g) * scale).to(torch.bfloat16)
 
-    if args.case in ("fc1", "fc2", "qkv", "out"):
-        n, k = {"fc1": (F, d), "fc2": (d, F), "qkv": (3 * d, d), "out": (d, d)}[args.case]
+    if args.case in ("fc1", "fc2", "qkv", "out", "fc1_e4m3", "fc2_e4m3", "qkv_e4m3"):
+        base = args.case.replace("_e4m3", "")
+        n, k = {"fc1": (F, d), "fc2": (d, F), "qkv": (3 * d, d), "out": (d, d)}[base]
         a, w = rnd(M, k), rnd(n, k, scale=0.02)
         bias = torch.zeros(n, device="cuda")
-        resid = rnd(M, n) if args.case in ("out", "fc2") else None     # the encoder's residual epilogue
-        fn = lambda: wb.linear(a, w, bias=bias, gelu=args.case == "fc1", resid=resid)  # noqa: E731
+        resid = rnd(M, n) if base in ("out", "fc2") else None           # the encoder's residual epilogue
+        if args.case.endswith("_e4m3"):
+            # E4M3 operands with per-tensor scales (the mixed_fp8 qkv / ffn sites)
+            (qa, sa), (qw, sw) = wb.quantize_fp8(a), wb.quantize_fp8(w)
+            fn = lambda: wb.linear(qa, qw, bias=bias, scale_a=sa, scale_w=sw, gelu=base == "fc1",  # noqa: E731
+                                   resid=resid)
+        else:
+            fn = lambda: wb.linear(a, w, bias=bias, gelu=base == "fc1", resid=resid)  # noqa: E731
         flops = 2.0 * M * n * k
     elif args.case == "attention":
         q, k_, v = rnd(B, 1500, d), rnd(B, 1500, d), rnd(B, 1500, d)
@@ -365,8 +372,8 @@ def main() -> None:
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="skip the batch-1 CUDA-graph and 45-minute long-form workloads timed after the bf16 step")
     ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph of the three calls")
-    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "attention", "layernorm", "layernorm_e4m3", "logmel",
-                                       "longform"),
+    ap.add_argument("--case", choices=("fc1", "fc2", "qkv", "out", "fc1_e4m3", "fc2_e4m3", "qkv_e4m3", "attention",
+                                       "layernorm", "layernorm_e4m3", "logmel", "longform"),
                     default=None,
                     help="launch one kernel class at full size (for profiler captures) instead of the bench")
     args = ap.parse_args()
