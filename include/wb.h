@@ -132,6 +132,18 @@ wb_status wb_check_device_error(void* stream, uint32_t* detail);
 /* Wait site that wb_selftest_wait_timeout() records (bits 8..15 of the word). */
 #define WB_SELFTEST_WAIT_SITE 0x7Fu
 
+/* Site that wb_selftest_bounds_check() records (bits 8..15 of the word). */
+#define WB_SELFTEST_BOUNDS_SITE 0x7Eu
+
+/* Diagnostic of the debug bounds checks (no memory touched).  Launches one
+ * kernel on `stream` that evaluates a bounds check on an index just past the
+ * extent it states.  In a debug build (wb_debug_build() == 1) the check fails
+ * and records the bounds bit and WB_SELFTEST_BOUNDS_SITE in the device error
+ * word, so the next wb_check_device_error() returns WB_EBOUNDS; a release
+ * build compiles the check away and records nothing.  Returns WB_ECUDA if the
+ * launch fails, else WB_OK (asynchronously). */
+wb_status wb_selftest_bounds_check(void* stream);
+
 /* Diagnostic of the bounded-wait path (no compute).  Launches one kernel on
  * `stream` whose single thread waits on an mbarrier that nothing arrives on.
  * The wait gives up after its time limit (about 2 s), sets the timeout bit and

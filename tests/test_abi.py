@@ -40,6 +40,7 @@ def test_header_constants_match_binding():
     src = open(os.path.join(ROOT, "include", "wb.h")).read()
     consts = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"#define\s+(WB_[A-Z0-9_]+)\s+(0x[0-9A-Fa-f]+|\d+)u?\b", src)}
     assert consts["WB_SELFTEST_WAIT_SITE"] == _lib.WB_SELFTEST_WAIT_SITE
+    assert consts["WB_SELFTEST_BOUNDS_SITE"] == _lib.WB_SELFTEST_BOUNDS_SITE
     assert consts["WB_LOGMEL_STATIC_MAX_CHUNKS"] == _lib.WB_LOGMEL_STATIC_MAX_CHUNKS
     assert 0 < _lib.WB_SELFTEST_WAIT_SITE < 256   # bits 8..15 of the error word
 

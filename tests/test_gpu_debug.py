@@ -201,3 +201,17 @@ def test_cross_kv_tiny(libs, wb):
         assert lib.wb_cross_kv(ctypes.c_void_p(enc_out.data_ptr()), 2, ctypes.byref(ds), 2, arr, kv.p, _stream()) == 0
         return [kv]
     _run_both(libs, fn)
+
+
+def test_bounds_check_selftest_reports_in_debug_build_only(libs):
+    # the reporting path of a failed check, end to end, without any out-of-range access: the debug
+    # build records the bounds bit and the self-test site, the release build records nothing
+    from whisper_encoder_gb300 import _lib
+    for name, lib in libs.items():
+        assert lib.wb_selftest_bounds_check(_stream()) == 0
+        st, word = _check_word(lib)
+        if name == "debug":
+            assert st == _lib.WB_EBOUNDS and word == (2 | (_lib.WB_SELFTEST_BOUNDS_SITE << 8)), (st, hex(word))
+            assert _check_word(lib) == (0, 0)            # reading cleared it
+        else:
+            assert (st, word) == (0, 0)

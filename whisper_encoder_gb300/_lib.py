@@ -17,6 +17,7 @@ WB_OK, WB_EINVAL, WB_ECUDA, WB_EUNSUPPORTED, WB_ETIMEOUT, WB_EWORKSPACE, WB_EBOU
 WB_BF16, WB_E4M3 = 0, 1
 WB_LOGMEL_STATIC_MAX_CHUNKS = 2   # include/wb.h
 WB_SELFTEST_WAIT_SITE = 0x7F      # include/wb.h
+WB_SELFTEST_BOUNDS_SITE = 0x7E    # include/wb.h
 
 c_int, c_i64, c_size, c_void, c_float = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 P = ctypes.POINTER
@@ -65,6 +66,7 @@ SIGNATURES = {
     "wb_debug_build": (c_int, []),
     "wb_check_device_error": (c_int, [c_void, P(ctypes.c_uint32)]),
     "wb_selftest_wait_timeout": (c_int, [c_void]),
+    "wb_selftest_bounds_check": (c_int, [c_void]),
     "wb_logmel_workspace_bytes": (c_size, [c_int, c_int]),
     "wb_logmel": (c_int, [c_void, c_i64, c_i64, c_int, c_int, c_void, c_void, c_size, c_void]),
     "wb_logmel_static": (c_int, [c_void, c_i64, c_i64, c_int, c_int, c_void, c_void]),

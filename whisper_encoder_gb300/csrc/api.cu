@@ -367,6 +367,12 @@ wb_status wb_check_device_error(void* stream, uint32_t* detail) {
   return (word & ERR_BOUNDS) ? WB_EBOUNDS : WB_OK;
 }
 
+wb_status wb_selftest_bounds_check(void* stream) {
+  if (!simt_err_ptr()) return WB_ECUDA;
+  WB_CUDA(launch_bounds_check_selftest(WB_SELFTEST_BOUNDS_SITE, static_cast<cudaStream_t>(stream)));
+  return WB_OK;
+}
+
 wb_status wb_selftest_wait_timeout(void* stream) {
   uint32_t* e = err_ptr();
   if (!e) return WB_ECUDA;

@@ -58,6 +58,7 @@ cudaError_t launch_zero_rows(__nv_bfloat16* base, long long row_elems, long long
                              int batch, int row, cudaStream_t s);
 cudaError_t launch_pos_table(float* pos, int T, int d, cudaStream_t s);
 cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint32_t site, cudaStream_t s);
+cudaError_t launch_bounds_check_selftest(uint32_t site, cudaStream_t s);
 // Device address of the error word of the SIMT kernels' debug bounds checks (per device, looked up
 // once); null if it cannot be found.
 uint32_t* simt_err_ptr();

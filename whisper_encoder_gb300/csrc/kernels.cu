@@ -977,6 +977,18 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint32_t site, cudaStrea
   return cudaGetLastError();
 }
 
+// Diagnostic of the debug bounds checks: evaluates one check on an index outside the stated extent
+// (11 of 10 elements).  Nothing is read or written but the error word: a debug build records
+// ERR_BOUNDS with the site, a release build compiles the check away and records nothing.
+__global__ void bounds_check_selftest_kernel(uint32_t site) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) (void)in_bounds(&g_simt_err, 10, 1, 10, site);
+}
+
+cudaError_t launch_bounds_check_selftest(uint32_t site, cudaStream_t s) {
+  bounds_check_selftest_kernel<<<1, 32, 0, s>>>(site);
+  return cudaGetLastError();
+}
+
 uint32_t* simt_err_ptr() {
   constexpr int kMaxDev = 64;
   static uint32_t* ptrs[kMaxDev] = {nullptr};
