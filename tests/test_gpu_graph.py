@@ -100,3 +100,22 @@ def test_encode_host_matches_oracle(wb):
         for b in range(2):
             ref = oenc.encoder(oenc.conv_stem(ofe.log_mel(a[b], dims.n_mels), w), w, dims.n_heads)
             assert rel_l2(got[b].float().numpy().astype(np.float64), ref) < 3e-2
+
+
+def test_encode_host_mixed_fp8_and_25s_stride(wb):
+    # wb_encode_host with the mixed_fp8 preset and overlapping 30 s windows at a 25 s stride (the
+    # long-form layout): bitwise the eager calls on the same windows
+    dims = synthetic.TINY
+    stem, enc = wb.upload_weights(synthetic.encoder_weights(dims, synthetic.SEED_TINY, "f32"))
+    B, stride = 2, 400000
+    pipe = wb.Pipeline(dims, stem, enc, batch=B, precision=wb.PRESET_MIXED_FP8)
+    n_samples = (B - 1) * stride + 480000 - 1234          # the last window runs past the end (zero fill)
+    batches = [synthetic.long_audio(3100 + i, n_samples) for i in range(3)]
+    host_in = [torch.from_numpy(a).pin_memory() for a in batches]
+    host_out = [torch.empty(pipe.out.shape, dtype=torch.bfloat16).pin_memory() for _ in batches]
+    pipe.run_host(host_in, host_out, chunk_stride=stride)
+    torch.cuda.synchronize()
+    assert wb.check_device_error() == 0
+    for a, got in zip(batches, host_out):
+        ref = pipe(torch.from_numpy(a).cuda(), chunk_stride=stride).cpu()
+        assert torch.equal(got, ref)
