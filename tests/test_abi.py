@@ -168,3 +168,22 @@ def test_product_and_oracle_share_no_code():
     src = open(os.path.join(ROOT, "synthetic", "__init__.py")).read()
     for word in ("fft", "mel_", "log10", "softmax", "layer_norm", "erf"):
         assert word not in src, word
+
+
+def test_header_is_plain_c(tmp_path):
+    # include/wb.h must serve C callers: it compiles as C99 on its own (no CUDA headers, no C++), and
+    # every function it declares has a prototype a C translation unit can take the address of
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "use_wb.c"
+    src.write_text('#include "wb.h"\n#include <stdio.h>\nint main(void) {\n  void* fns[] = {\n'
+                   + "".join(f"    (void*){n},\n" for n in names)
+                   + '  };\n  printf("%d\\n", (int)(sizeof(fns) / sizeof(fns[0])));\n  return 0;\n}\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-Wno-pedantic",
+                        "-I" + os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_wb.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
