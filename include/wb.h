@@ -40,7 +40,7 @@ typedef enum {
   WB_OK = 0,
   WB_EINVAL = -1,        /* bad pointer, size or layout argument */
   WB_ECUDA = -2,         /* a CUDA runtime/driver call or launch failed */
-  WB_EUNSUPPORTED = -3,  /* valid request this build does not implement (e.g. mixed bf16 x E4M3 site) */
+  WB_EUNSUPPORTED = -3,  /* valid request this library does not implement (e.g. mixed bf16 x E4M3 site) */
   WB_ETIMEOUT = -4,      /* a bounded device-side wait ran out (reported by wb_check_device_error) */
   WB_EWORKSPACE = -5,    /* workspace pointer null or smaller than the *_workspace_bytes() query */
   WB_EBOUNDS = -6        /* debug builds only: a kernel index fell outside its buffer (wb_check_device_error) */
