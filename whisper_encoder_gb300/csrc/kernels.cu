@@ -688,25 +688,43 @@ __global__ void dequantize_kernel(const uint8_t* __restrict__ q, const float* __
 }
 
 // v [batch*T][ld] (head h at columns 64h..64h+63) -> f16 vt [(b*H + h)*64 + e][T_PAD]
-__global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, long long ld, int T, int H,
-                                   __half* __restrict__ vt) {
-  __shared__ __nv_bfloat16 tile[32][34];
-  const int b = blockIdx.z;
-  const int t0 = blockIdx.x * 32, c0 = blockIdx.y * 32;  // c over H*64 columns
-  for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
-    const int t = t0 + ty;
-    const long long vi = (static_cast<long long>(b) * T + t) * ld + c0 + threadIdx.x;
-    tile[ty][threadIdx.x] = t < T && WB_IN(vi, 1, static_cast<long long>(gridDim.z) * T * ld, SITE_TRANSPOSE_V_IN)
-                                ? v[vi]
-                                : __float2bfloat16_rn(0.0f);
+static_assert(T_PAD % 8 == 0, "V^T rows are written in 8-position vectors");
+
+// V [batch][T][ld] (bf16, head h in columns 64h .. 64h + 63) -> V^T [batch * H][64][T_PAD] (f16).
+// A block moves a 128-position x 64-column tile of one head; each thread reads an 8 x 8 block as eight
+// 16-byte row segments, transposes it in registers and writes eight 16-byte segments of V^T rows, so
+// every global access is a full 16-byte vector (a warp's loads cover four 128-byte row segments).
+// Positions T .. T_PAD - 1 of a V^T row are written as zeros.
+__global__ void __launch_bounds__(128) transpose_v_kernel(const __nv_bfloat16* __restrict__ v, long long ld, int T,
+                                                          int H, __half* __restrict__ vt) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int ty = threadIdx.x >> 3, cg = threadIdx.x & 7;    // 16 row groups x 8 column groups
+  const int t0 = blockIdx.x * 128 + ty * 8;                  // first of this thread's 8 positions
+  if (t0 >= T_PAD) return;
+  const long long in_el = static_cast<long long>(gridDim.z) * T * ld;
+  uint4 r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const long long vi = (static_cast<long long>(b) * T + t0 + i) * ld + h * 64 + cg * 8;
+    r[i] = (t0 + i < T && WB_IN(vi, 8, in_el, SITE_TRANSPOSE_V_IN))
+               ? *reinterpret_cast<const uint4*>(v + vi)
+               : make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
-  for (int ty = threadIdx.y; ty < 32; ty += blockDim.y) {
-    const int c = c0 + ty, t = t0 + threadIdx.x;
-    const int h = c >> 6, e = c & 63;
-    const long long oi = (static_cast<long long>(b * H + h) * 64 + e) * T_PAD + t;
-    if (t < T && WB_IN(oi, 1, static_cast<long long>(gridDim.z) * H * 64 * T_PAD, SITE_TRANSPOSE_V_OUT))
-      vt[oi] = __float2half_rn(__bfloat162float(tile[threadIdx.x][ty]));
+  const long long out_el = static_cast<long long>(gridDim.z) * H * 64 * T_PAD;
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) {
+    // column cg * 8 + jj of the eight rows: bf16 element jj of each row segment
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const uint32_t a = (&r[i].x)[jj >> 1], c = (&r[i + 1].x)[jj >> 1];
+      const uint32_t ba = (jj & 1) ? (a >> 16) : (a & 0xffffu), bc = (jj & 1) ? (c >> 16) : (c & 0xffffu);
+      const __half lo = __float2half_rn(__uint_as_float(ba << 16)), hi = __float2half_rn(__uint_as_float(bc << 16));
+      w[i >> 1] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+    }
+    const long long oi = (static_cast<long long>(b * H + h) * 64 + cg * 8 + jj) * T_PAD + t0;
+    if (WB_IN(oi, 8, out_el, SITE_TRANSPOSE_V_OUT))
+      *reinterpret_cast<uint4*>(vt + oi) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -940,8 +958,8 @@ cudaError_t launch_dequantize(const uint8_t* q, const float* scale, long long n,
 
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, long long ld, int batch, int T, int H, __half* vt,
                                cudaStream_t s) {
-  dim3 grid((T + 31) / 32, H * 2, batch);
-  transpose_v_kernel<<<grid, dim3(32, 8), 0, s>>>(v, ld, T, H, vt);
+  dim3 grid((T_PAD + 127) / 128, H, batch);
+  transpose_v_kernel<<<grid, 128, 0, s>>>(v, ld, T, H, vt);
   return cudaGetLastError();
 }
 
