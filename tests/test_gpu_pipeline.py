@@ -155,3 +155,35 @@ def test_encoder_is_deterministic(wb):
     a = wb.encoder_forward(x0, dims, enc)
     b = wb.encoder_forward(x0, dims, enc)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("case", ["tiny_b1", "large_b1", "large_b4_offset"])
+def test_layernorm_statistics_from_residual_epilogues(wb, case):
+    """Within one encoder call a folded LN1 / LN2 takes its row statistics from the epilogue of the
+    residual GEMM that wrote its input ((mean, M2) per 32-column group, merged per row by a short
+    pass); a call starting at a layer forms that layer's LN1 statistics with the row kernel.  Running
+    the layers in one call and one call per layer must therefore agree closely, and both must follow
+    the oracle.  The offset case gives every row a mean far above its spread."""
+    if case == "tiny_b1":
+        dims, batch, n_layers, offset = synthetic.TINY, 1, 3, 0.0
+    elif case == "large_b1":
+        dims, batch, n_layers, offset = synthetic.LARGE_V3, 1, 2, 0.0
+    else:
+        dims, batch, n_layers, offset = synthetic.LARGE_V3, 4, 2, 24.0
+    dims = synthetic.Dims(dims.n_mels, dims.d_model, dims.n_heads, n_layers, dims.d_ffn)
+    w = synthetic.encoder_weights(dims, synthetic.SEED_TINY + 7, "bf16", n_layers=n_layers)
+    _, enc = wb.upload_weights(w)
+    rng = np.random.default_rng(11)
+    x0 = rng.normal(0.0, 1.0, (batch, 1500, dims.d_model)) + offset
+    x0d = torch.as_tensor(x0, dtype=torch.float32).to(DEV).to(torch.bfloat16)
+    whole = to_np(wb.encoder_forward(x0d, dims, enc, final_ln=False))
+    h = x0d
+    for layer in range(n_layers):
+        h = wb.encoder_forward(h, dims, enc, layer_begin=layer, layer_end=layer + 1, final_ln=False)
+    stepwise = to_np(h)
+    assert wb.check_device_error() == 0
+    for b in range(batch):
+        d = rel_l2(whole[b], stepwise[b])
+        assert d < 2e-3, (b, d)
+    ref = oenc.encoder(to_np(x0d)[0], w, dims.n_heads, final_ln=False)
+    assert rel_l2(whole[0], ref) < n_layers * LAYER_TOL

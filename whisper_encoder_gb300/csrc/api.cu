@@ -234,7 +234,7 @@ bool dims_ok(const wb_dims* d) {
 bool site_ok(int w, int a) { return (w == WB_BF16 || w == WB_E4M3) && w == a; }
 
 struct EncLayout {
-  size_t h, a, qk, vt, o, g, aq, gq, slots, stats, total;
+  size_t h, a, qk, vt, o, g, aq, gq, slots, stats, ln_part, total;
 };
 
 EncLayout enc_layout(const wb_dims* d, int batch, const wb_precision* pr) {
@@ -256,6 +256,8 @@ EncLayout enc_layout(const wb_dims* d, int batch, const wb_precision* pr) {
   L.slots = c.take(static_cast<size_t>(4) * (d->n_layers > 0 ? d->n_layers : 1) * batch * sizeof(float));
   // LayerNorm row statistics (mean, rstd) for a folded LN1 / LN2 site
   L.stats = c.take(M * sizeof(float2));
+  // (mean, M2) per row and 32-column group, left by the residual GEMMs' epilogues
+  L.ln_part = c.take(M * (D / 32) * sizeof(float2));
   L.total = c.off;
   return L;
 }
@@ -623,6 +625,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
   auto* gq = pr.ffn_a == WB_E4M3 ? reinterpret_cast<uint8_t*>(ws + EL.gq) : nullptr;
   auto* slots = reinterpret_cast<float*>(ws + EL.slots);
   auto* stats = reinterpret_cast<float2*>(ws + EL.stats);
+  auto* ln_part = reinterpret_cast<float2*>(ws + EL.ln_part);
   const auto* x0b = static_cast<const __nv_bfloat16*>(x0);
   auto* outb = static_cast<__nv_bfloat16*>(out);
   const float eps = 1e-5f;
@@ -636,6 +639,16 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
   };
   auto fold_fc1 = [&](int l) {
     return pr.ffn_a == WB_BF16 && layers[l].w_fc1_ln && layers[l].c_fc1 && layers[l].b_fc1_ln;
+  };
+  // A folded LayerNorm's statistics come from the residual GEMM that writes its input (out-projection
+  // for LN2, the previous layer's FC2 for LN1): its epilogue leaves (mean, M2) per row and column
+  // group and a short pass merges them, instead of a pass that reads the whole activation again.  The
+  // first layer's LN1 reads the stem output with the statistics kernel.
+  const bool stats_in_epi = D % 32 == 0;
+  bool stats_ready = false;   // the previous FC2 has left the partial statistics of this layer's input
+  auto merge_stats = [&]() -> cudaError_t {
+    Prof pr(PC_ENC_LN, s);
+    return launch_ln_merge(ln_part, M, D / 32, 32, eps, stats, s);
   };
 
   for (int l = layer_begin; l < layer_end; ++l) {
@@ -652,13 +665,18 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
     const bool fq = fold_qkv(l), ff = fold_fc1(l);
     // LN1 -> a  [-> E4M3]  (folded: only the row statistics; QKV reads src itself)
     {
-      Prof pr(PC_ENC_LN, s, !fq && q8 ? 2 : 1);
-      if (fq)
+      if (fq && stats_ready) {
+        WB_CUDA(merge_stats());
+      } else if (fq) {
+        Prof pr(PC_ENC_LN, s);
         WB_CUDA(launch_ln_stats(src, M, D, eps, stats, s));
-      else if (q8)   // E4M3 operand: LayerNorm writes the codes itself
+      } else if (q8) {
+        Prof pr(PC_ENC_LN, s, 2);   // E4M3 operand: LayerNorm writes the codes itself
         WB_CUDA(launch_layernorm_e4m3(src, W.ln1_g, W.ln1_b, M, D, eps, stats, am_qkv, T_TOK, aq, s));
-      else
+      } else {
+        Prof pr(PC_ENC_LN, s);
         WB_CUDA(launch_layernorm(src, nullptr, W.ln1_g, W.ln1_b, M, D, eps, a, nullptr, s));
+      }
     }
     {  // QKV projection: q | k to qk [M, 2D], v transposed to vt
       GemmParams p = base_params();
@@ -693,6 +711,7 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
       Prof pr(PC_ENC_QUANT, s);
       WB_CUDA(launch_quantize_rows(o, static_cast<long long>(M) * D, D, T_TOK, am_out, aq, s));
     }
+    const bool ln2_in_epi = ff && stats_in_epi;
     {  // out projection + bias + residual -> h
       GemmParams p = base_params();
       p.bias = W.b_out;
@@ -700,14 +719,19 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.amax_a = am_out;
         p.scale_b = W.s_out;
       }
+      if (ln2_in_epi) p.ln_part = ln_part;
       wb_status st = dense_gemm(o8 ? static_cast<const void*>(aq) : o, W.w_out, M, D, D, o8, EPI_BIAS_RESID, h, D, D,
                                 src, p, s, PC_ENC_OUT);
       if (st != WB_OK) return st;
     }
     // LN2 -> a [-> E4M3]  (folded: only the row statistics; FC1 reads h itself)
     if (ff) {
-      Prof pr(PC_ENC_LN, s);
-      WB_CUDA(launch_ln_stats(h, M, D, eps, stats, s));
+      if (ln2_in_epi) {
+        WB_CUDA(merge_stats());
+      } else {
+        Prof pr(PC_ENC_LN, s);
+        WB_CUDA(launch_ln_stats(h, M, D, eps, stats, s));
+      }
     } else if (f8) {
       Prof pr(PC_ENC_LN, s, 2);
       WB_CUDA(launch_layernorm_e4m3(h, W.ln2_g, W.ln2_b, M, D, eps, stats, am_fc1, T_TOK, aq, s));
@@ -747,6 +771,8 @@ wb_status wb_encoder_forward(const void* x0, int batch, const wb_dims* dims, con
         p.scale_b = W.s_fc2;
       }
       void* dst = (last && !apply_final_ln) ? static_cast<void*>(outb) : static_cast<void*>(h);
+      stats_ready = !last && fold_qkv(l + 1) && stats_in_epi;
+      if (stats_ready) p.ln_part = ln_part;
       wb_status st = dense_gemm(f8 ? static_cast<const void*>(gq) : g, W.w_fc2, M, D, F, f8, EPI_BIAS_RESID, dst, D, D,
                                 h, p, s, PC_ENC_FC2);
       if (st != WB_OK) return st;

@@ -327,11 +327,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
-          if (p.amax && row_ok) {   // packed |bf16| maxima, folded to one float per chunk
-            uint32_t mx2 = 0u;
+          if (EPI == EPI_BIAS_RESID && p.ln_part && row_ok) {
+            // the next LayerNorm's statistics: (mean, M2) of these 32 outputs (before their bf16
+            // rounding), accumulated about the first of them (so that the sums do not cancel), for a
+            // pass that merges each row's N / 32 groups once the whole output is written (the same
+            // groups at every tile width)
+            const float k0 = __uint_as_float(pk[0] << 16);
+            const uint64_t one2 = f32x2_pack(1.0f, 1.0f), nk2 = f32x2_pack(-k0, -k0);
+            uint64_t s1 = f32x2_pack(0.0f, 0.0f), s2 = s1;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) mx2 = bf16x2_max(mx2, pk[i] & 0x7fff7fffu);
-            tile_amax = fmaxf(tile_amax, fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xffff0000u)));
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t d2 =
+                  f32x2_fma(f32x2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)), one2, nk2);
+              s1 = f32x2_fma(d2, one2, s1);
+              s2 = f32x2_fma(d2, d2, s2);
+            }
+            float a0, a1, q0, q1;
+            f32x2_unpack(s1, a0, a1);
+            f32x2_unpack(s2, q0, q1);
+            const float sd = a0 + a1;
+            // group-major, so that a warp's 32 rows write 256 contiguous bytes
+            const long long rows_all = static_cast<long long>(p.batch) * p.M;
+            const long long pi = static_cast<long long>(n0 >> 5) * rows_all + static_cast<long long>(b) * p.M + m;
+            if (in_bounds(p.err, pi, 1, rows_all * (p.N >> 5), SITE_GEMM_LNPART))
+              p.ln_part[pi] = make_float2(k0 + sd * (1.0f / 32.0f), fmaxf((q0 + q1) - sd * sd * (1.0f / 32.0f), 0.0f));
           }
           if (lane == 0) bulk_wait_read0();       // the previous store has read the staging box
           __syncwarp();

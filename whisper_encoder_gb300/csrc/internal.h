@@ -38,6 +38,8 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* res, con
 cudaError_t launch_layernorm_e4m3(const __nv_bfloat16* x, const float* g, const float* b, int rows, int d, float eps,
                                   float2* stats, float* amax, int rows_per_item, uint8_t* q, cudaStream_t s);
 cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s);
+cudaError_t launch_ln_merge(const float2* part, long long rows, int n_groups, int group, float eps, float2* out,
+                            cudaStream_t s);
 cudaError_t launch_fold_ln(const __nv_bfloat16* w, const float* b, const float* gamma, const float* beta, int n_out,
                            int d, __nv_bfloat16* w_ln, float* c, float* b_ln, cudaStream_t s);
 cudaError_t launch_quantize_e5m2(const __nv_bfloat16* x, long long n, uint8_t* q, float* amax_to_scale,

@@ -884,6 +884,61 @@ static cudaError_t ln_stats_launch(const __nv_bfloat16* x, int rows, float eps, 
                     static_cast<float*>(nullptr), 1);
 }
 
+// (mean, rstd) of each row from the (mean, M2) of its n_groups column groups of `group` values each,
+// stored group-major (part[g * rows + r]) as the residual GEMM epilogues leave them, merged about the
+// first group's mean (the pairwise update of Chan, Golub and LeVeque for equal counts).  A block
+// takes 32 rows: warp w sums the groups w, w + 8, .. of the 32 rows (each load 256 contiguous bytes)
+// and shared memory adds the eight warps' sums.
+constexpr int MERGE_SLICES = 8;
+__global__ void __launch_bounds__(32 * MERGE_SLICES) ln_merge_kernel(const float2* __restrict__ part, int rows,
+                                                                     int n_groups, int group, float eps,
+                                                                     float2* __restrict__ stats) {
+  __shared__ float red[3][MERGE_SLICES][33];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const long long row = static_cast<long long>(blockIdx.x) * 32 + lane;
+  const long long n_el = static_cast<long long>(rows) * n_groups;
+  float s1 = 0.0f, s2 = 0.0f, s3 = 0.0f, m0 = 0.0f;
+  if (row < rows) {
+    m0 = WB_IN(row, 1, n_el, SITE_LNMERGE_IN) ? part[row].x : 0.0f;
+    for (int gi = w; gi < n_groups; gi += MERGE_SLICES) {
+      const long long i = static_cast<long long>(gi) * rows + row;
+      if (!WB_IN(i, 1, n_el, SITE_LNMERGE_IN)) continue;
+      const float2 t = part[i];
+      const float dl = t.x - m0;
+      s1 += dl;
+      s2 = fmaf(dl, dl, s2);
+      s3 += t.y;
+    }
+  }
+  red[0][w][lane] = s1;
+  red[1][w][lane] = s2;
+  red[2][w][lane] = s3;
+  __syncthreads();
+  if (w != 0 || row >= rows) return;
+  s1 = s2 = s3 = 0.0f;
+#pragma unroll
+  for (int k = 0; k < MERGE_SLICES; ++k) {
+    s1 += red[0][k][lane];
+    s2 += red[1][k][lane];
+    s3 += red[2][k][lane];
+  }
+  if (WB_IN(row, 1, rows, SITE_LNMERGE_OUT)) {
+    const float ng = static_cast<float>(n_groups);
+    const float m2 = s3 + static_cast<float>(group) * fmaxf(s2 - s1 * s1 / ng, 0.0f);
+    stats[row] = make_float2(m0 + s1 / ng, rsqrtf(m2 / (ng * static_cast<float>(group)) + eps));
+  }
+}
+
+cudaError_t launch_ln_merge(const float2* part, long long rows, int n_groups, int group, float eps, float2* out,
+                            cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (rows >= (1LL << 31) || n_groups < 1 || group < 1) return cudaErrorInvalidValue;
+  return launch_pdl(ln_merge_kernel, dim3(static_cast<unsigned>((rows + 31) / 32)), dim3(32 * MERGE_SLICES), 0, s,
+                    part, static_cast<int>(rows), n_groups, group, eps, out);
+}
+
 cudaError_t launch_ln_stats(const __nv_bfloat16* x, long long rows, int d, float eps, float2* out, cudaStream_t s) {
   // widths that are multiples of 128 (every Whisper size): the persistent row walk
   if (rows > 0 && rows < (1LL << 31)) {

@@ -55,6 +55,10 @@ struct GemmParams {
   // forms rstd (acc - mean ln_c[n]) + bias[n]
   const float2* ln_stats;
   const float* ln_c;
+  // EPI_BIAS_RESID: if set, per output row r (of batch * M) and 32-column group g,
+  // ln_part[g * batch * M + r] = (mean, M2) of the group's stored (bf16) values: the next
+  // LayerNorm's statistics, before merging
+  float2* ln_part;
   float* amax;               // if set: per-item atomic max of |y| (feeds the next E4M3 operand's scale)
   const float* pos;          // EPI_CONV2: position table [M][N] (float32), added after the GELU
   // QKV: columns >= vt_col0 are written transposed, as f16, to vt[(b*H + h)*64 + e][t]
@@ -117,8 +121,9 @@ enum : uint32_t {
   SITE_ZERO_ROWS, SITE_PACK_CONV, SITE_LN_X, SITE_LN_Y, SITE_LN_GB, SITE_STATS_X, SITE_STATS_OUT,
   SITE_STATS_AMAX, SITE_LNQ_X, SITE_LNQ_Q, SITE_LNQ_AUX, SITE_ROWSTATS, SITE_FOLD, SITE_QUANT,
   SITE_QUANT_ROWS, SITE_E5M2, SITE_DEQUANT, SITE_TRANSPOSE_V_IN, SITE_TRANSPOSE_V_OUT, SITE_POS, SITE_AMAX,
+  SITE_LNMERGE_IN, SITE_LNMERGE_OUT,
   SITE_GEMM_RESID = 0x40, SITE_GEMM_BIAS, SITE_GEMM_LNSTATS, SITE_GEMM_POS, SITE_GEMM_VT, SITE_GEMM_POWER,
-  SITE_GEMM_MEL, SITE_GEMM_AMAX,
+  SITE_GEMM_MEL, SITE_GEMM_AMAX, SITE_GEMM_LNPART,
   SITE_ATT_OUT = 0x50, SITE_ATT_AMAX
 };
 
