@@ -273,8 +273,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               } else if (FP8) {
                 f32x2_unpack(f32x2_fma(acc2, f32x2_pack(alpha, alpha), b2), x0, x1);
               } else {
-                x0 = v[4 * i4 + kk] + bv[kk];
-                x1 = v[4 * i4 + kk + 1] + bv[kk + 1];
+                f32x2_unpack(f32x2_fma(acc2, f32x2_pack(1.0f, 1.0f), b2), x0, x1);   // one rounding, as x + b
               }
               if (EPI == EPI_BIAS_GELU || EPI == EPI_CONV2 || (EPI == EPI_BIAS_RESID && p.act_gelu)) {
                 // measured: the packed form is faster where the main loop bounds the tile (bf16) and
@@ -317,11 +316,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             continue;
           }
           if constexpr (EPI == EPI_BIAS_RESID) {
+            // residual pairs: bf16 -> fp32 by shifts, added with packed fp32 pairs (one rounding each)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&rres[4 * c + j]);
+              const uint32_t rw[4] = {rres[4 * c + j].x, rres[4 * c + j].y, rres[4 * c + j].z, rres[4 * c + j].w};
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[8 * j + i] += __bfloat162float(hv[i]);
+              for (int i = 0; i < 4; ++i) {
+                const uint64_t r2 = f32x2_pack(__uint_as_float(rw[i] << 16), __uint_as_float(rw[i] & 0xffff0000u));
+                f32x2_unpack(f32x2_fma(f32x2_pack(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]), f32x2_pack(1.0f, 1.0f), r2),
+                             v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+              }
             }
           }
           uint32_t pk[16];
