@@ -97,7 +97,10 @@ typedef struct {
   /* Optional LayerNorm folds made by wb_fold_layernorm (all three NULL: not folded).  When a bf16
    * QKV (FC1) site has them, the forward skips the LN1 (LN2) pass: the GEMM reads the residual
    * stream itself with w_*_ln and the epilogue applies the row's mean and rstd (see
-   * wb_fold_layernorm).  E4M3 sites ignore them. */
+   * wb_fold_layernorm).  Those statistics come from the residual GEMM that wrote the stream (the
+   * out-projection for LN2, the previous layer's FC2 for LN1: per 32-column group, merged per row
+   * by a short pass); the first layer of a call forms its LN1 statistics with a pass over x0.
+   * E4M3 sites ignore them. */
   const void* w_qkv_ln;  const float* c_qkv;  const float* b_qkv_ln;  /* bf16 [3d, d], f32 [3d], [3d] */
   const void* w_fc1_ln;  const float* c_fc1;  const float* b_fc1_ln;  /* bf16 [F, d],  f32 [F],  [F]  */
 } wb_layer_weights;
