@@ -332,10 +332,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
           if (EPI == EPI_BIAS_RESID && p.ln_part && row_ok) {
-            // the next LayerNorm's statistics: (mean, M2) of these 32 outputs (before their bf16
-            // rounding), accumulated about the first of them (so that the sums do not cancel), for a
-            // pass that merges each row's N / 32 groups once the whole output is written (the same
-            // groups at every tile width)
+            // the next LayerNorm's statistics: (mean, M2) of these 32 stored (bf16) outputs,
+            // accumulated about the first of them (so that the sums do not cancel), for a pass that
+            // merges each row's N / 32 groups once the whole output is written (the same groups at
+            // every tile width)
             const float k0 = __uint_as_float(pk[0] << 16);
             const uint64_t one2 = f32x2_pack(1.0f, 1.0f), nk2 = f32x2_pack(-k0, -k0);
             uint64_t s1 = f32x2_pack(0.0f, 0.0f), s2 = s1;
