@@ -299,9 +299,10 @@ wb_status run_attention(const __nv_bfloat16* q, const __nv_bfloat16* k, long lon
   CUtensorMap qm, km, vm;
   const uint64_t qdims[3] = {d, static_cast<uint64_t>(T), static_cast<uint64_t>(batch)};
   const uint64_t qstr[2] = {static_cast<uint64_t>(ld_qk) * 2, static_cast<uint64_t>(ld_qk) * 2 * T};
-  const uint32_t qbox[3] = {64, 128, 1};
+  const uint32_t qbox[3] = {64, ATT_BQ, 1};
+  const uint32_t kbox[3] = {64, ATT_BKV, 1};
   if (!make_map(&qm, false, 3, q, qdims, qstr, qbox)) return WB_ECUDA;
-  if (!make_map(&km, false, 3, k, qdims, qstr, qbox)) return WB_ECUDA;
+  if (!make_map(&km, false, 3, k, qdims, qstr, kbox)) return WB_ECUDA;
   const uint64_t vdims[3] = {static_cast<uint64_t>(T), 64, static_cast<uint64_t>(batch) * H};
   const uint64_t vstr[2] = {static_cast<uint64_t>(T_PAD) * 2, static_cast<uint64_t>(T_PAD) * 2 * 64};
   const uint32_t vbox[3] = {64, 64, 1};
