@@ -187,3 +187,28 @@ def test_layernorm_statistics_from_residual_epilogues(wb, case):
         assert d < 2e-3, (b, d)
     ref = oenc.encoder(to_np(x0d)[0], w, dims.n_heads, final_ln=False)
     assert rel_l2(whole[0], ref) < n_layers * LAYER_TOL
+
+
+def test_ffn_e4m3_with_folded_bf16_qkv(wb):
+    """A per-site mix the presets do not cover: QKV and out-projection in bf16 (LN1 folded into QKV,
+    its statistics formed by the previous layer's FC2, here an E4M3 GEMM), FFN in E4M3.  Each layer
+    from the oracle's own input within 6e-2 of the oracle with E4M3 at the ffn site only."""
+    dims = synthetic.Dims(synthetic.TINY.n_mels, synthetic.TINY.d_model, synthetic.TINY.n_heads, 3,
+                          synthetic.TINY.d_ffn)
+    w = synthetic.encoder_weights(dims, synthetic.SEED_TINY + 9, "bf16", n_layers=3)
+    _, enc = wb.upload_weights(w)
+    enc.quantize()
+    prec = (wb.WB_BF16, wb.WB_BF16, wb.WB_BF16, wb.WB_BF16, wb.WB_E4M3, wb.WB_E4M3)
+    rng = np.random.default_rng(13)
+    x0 = synthetic.round_to(rng.normal(0.0, 1.0, (1500, dims.d_model)).astype(np.float32), "bf16")
+    whole = to_np(wb.encoder_forward(_dev(x0[None]).to(torch.bfloat16), dims, enc, precision=prec,
+                                     final_ln=False))[0]
+    assert wb.check_device_error() == 0
+    h = x0.astype(np.float64)
+    for layer in range(3):
+        nxt = oenc.encoder_layer(h, w["layers"][layer], dims.n_heads, fp8_sites=("ffn",))
+        got = to_np(wb.encoder_forward(_dev(h[None]).to(torch.bfloat16), dims, enc, precision=prec,
+                                       layer_begin=layer, layer_end=layer + 1, final_ln=False))[0]
+        assert rel_l2(got, nxt) < FP8_TOL, layer
+        h = nxt
+    assert rel_l2(whole, h) < FP8_TOL
