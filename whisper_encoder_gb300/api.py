@@ -426,7 +426,8 @@ class Pipeline:
 
         ``graph.replay()`` then recomputes ``self.out`` from the buffer's current contents with
         one launch instead of ~240 (the calls synchronize nothing and allocate nothing, so
-        they can be captured; two eager warm-up calls run first)."""
+        they can be captured; two eager warm-up calls run first).  The graph reads and writes
+        this pipeline's buffers: keep the Pipeline (and ``audio``) alive while it is replayed."""
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
